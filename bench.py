@@ -1,0 +1,431 @@
+"""Benchmark of the BDLM attention hot path on GB300.
+
+One step = the whole hot path over one synthetic 128K + 128K sequence
+(32 query heads / 8 kv heads, head_dim 128, block 64):
+  tile enumeration -> 8 partial forwards against contiguous clean-K/V shards
+  + 1 partial forward against the local corrupted K/V -> LSE merge of the 9
+  partials -> full backward (preprocess, key-major main kernel, dq convert).
+Metric: valid-pair TFLOP/s, FLOPs = 4*d*H*P (forward) + 10*d*H*P (backward),
+P = n(n + B) valid (query, key) pairs per head.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). With --gpus N > 1 (torchrun) every rank runs
+an independent replica of the step on its own GPU; the timing is the max over
+ranks and the value the FLOPs of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+WORKLOAD = synth.BY_NAME["long128k_n131072_b64_h32kv8_d128"]
+METRIC = "BDLM attn fwd+bwd TFLOP/s (valid pairs) and % BF16 peak at 128K, 1 GB300"
+UNIT = "TFLOP/s"
+
+# dram traffic of the dominant kernel per launch from an ncu capture, valid
+# while its source is unchanged (checked by hash; otherwise reported as null)
+TRAFFIC = {"kernel_source": None, "sha1": None, "bytes_per_launch": None, "note": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def valid_pairs(n, block):
+    return n * (n + block)
+
+
+def step_flops(w):
+    P = valid_pairs(w.n, w.block)
+    return 4 * w.head_dim * w.heads * P, 10 * w.head_dim * w.heads * P
+
+
+def merge_bytes(w, n_parts):
+    rows, per = 2 * w.n, w.heads
+    unit = 2 * w.head_dim + 4  # bf16 row of o + fp32 lse
+    return rows * per * unit * (n_parts + 1)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception as e:  # pragma: no cover
+            log("clock sampling unavailable:", e)
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+# ----------------------------------------------------------------------------
+# the oracle leg (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(x_host, w, budget_s):
+    """Run the float64 oracle (forward + backward) on query blocks of kv group
+    0 of the workload, latest blocks first (the heaviest rows), until budget_s
+    of CPU time is spent. Returns (valid pairs per second, pairs, seconds, blocks)."""
+    import numpy as np
+
+    import oracle
+
+    G = w.heads // w.kv_heads
+    q, k, v, do = x_host
+    n, B = w.n, w.block
+    nb = n // B
+    order = []
+    for b in range(nb - 1, -1, -1):
+        order += [(0, b * B), (0, n + b * B)]
+    t0 = time.perf_counter()
+    pairs = 0
+    done = 0
+    for blk in order:
+        oracle.bdlm_attention(q, k, v, B, w.scale, do=do, row_blocks=[blk])
+        b = (blk[1] % n) // B
+        pairs += B * (b + 1) * B * G
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return pairs / dt, pairs, dt, done
+
+
+def host_group0(x, w):
+    import numpy as np
+
+    G = w.heads // w.kv_heads
+    f = lambda t: t.float().cpu().numpy()
+    return (f(x.q[:, :G]), f(x.k[:, :1]), f(x.v[:, :1]), f(x.do[:, :G]))
+
+
+def oracle_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = WORKLOAD
+    # one kv group of the workload (G query heads, 1 kv head), same shapes and
+    # distributions, drawn on the CPU
+    G = w.heads // w.kv_heads
+    wg = synth.Workload(w.name + "_group0", n=w.n, block=w.block, heads=G, kv_heads=1, head_dim=w.head_dim,
+                        seed=w.seed, qkv_std=w.qkv_std)
+    x = synth.make_inputs(wg, device="cpu")
+    xh = host_group0(x, wg)
+    flop_per_pair = 14 * w.head_dim
+    for _ in range(args.warmup):
+        oracle_sample(xh, w, budget_s=0.5)
+    times, pairs = [], []
+    for _ in range(args.steps):
+        rate, pr, dt, nblk = oracle_sample(xh, w, budget_s=args.ref_budget)
+        times.append(dt)
+        pairs.append(pr)
+    total_pairs, total_t = sum(pairs), sum(times)
+    value = flop_per_pair * total_pairs / total_t / 1e12
+    sample = (f"float64 oracle fwd+bwd on the latest query blocks (B={w.block} rows each, kv group 0 = "
+              f"{w.heads // w.kv_heads} q heads) of the 128K workload, ~{args.ref_budget:.0f} s per step")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_pairs_per_step": total_pairs // args.steps},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the CUDA arm
+# ----------------------------------------------------------------------------
+class Step:
+    def __init__(self, bd, w, x, dev):
+        self.bd, self.w, self.x = bd, w, x
+        n, H, d = w.n, w.heads, w.head_dim
+        L = 2 * n
+        self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+        self.parts = [torch.empty_like(x.q) for _ in self.windows]
+        self.plse = [torch.empty((H, L), dtype=torch.float32, device=dev) for _ in self.windows]
+        self.o = torch.empty_like(x.q)
+        self.lse = torch.empty((H, L), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(x.q)
+        self.dk = torch.empty_like(x.k)
+        self.dv = torch.empty_like(x.v)
+        self.ws_f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d, 1), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d, 1), dtype=torch.uint8, device=dev)
+        self.launches = 0
+
+    def run(self, ev=None):
+        bd, w, x = self.bd, self.w, self.x
+        launches = 0
+        if ev:
+            ev[0].record()
+        for (lo, hi), po, pl in zip(self.windows, self.parts, self.plse):
+            bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], w.block, part=bd.Partial.window(lo, hi), out=po, lse=pl,
+                             workspace=self.ws_f)
+            launches += bd.bdlm_last_launch_count()
+        if ev:
+            ev[1].record()
+        bd.bdlm_lse_merge(self.parts, self.plse, out=self.o, lse=self.lse)
+        launches += bd.bdlm_last_launch_count()
+        if ev:
+            ev[2].record()
+        bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, dq=self.dq, dk=self.dk, dv=self.dv,
+                         workspace=self.ws_b)
+        launches += bd.bdlm_last_launch_count()
+        if ev:
+            ev[3].record()
+        self.launches += launches
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world, dev):
+    if world > 1:
+        import torch.distributed as dist
+
+        if dev.type == "cuda":
+            dist.barrier(device_ids=[dev.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_cuda(args, rank, world, local):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
+    bd.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    log(f"[rank {rank}] generating inputs for {w.name}")
+    x = synth.make_inputs(w, device="cuda")
+    step = Step(bd, w, x, dev)
+    f_fwd, f_bwd = step_flops(w)
+    flops = f_fwd + f_bwd
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    step.launches = 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for k in range(args.steps):
+        step.run(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launches = step.launches
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    mrg_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    bwd_ms = statistics.median(e[2].elapsed_time(e[3]) for e in evs)
+    bwd_mean_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / len(evs)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    value = flops * world * args.steps / (total_ms / 1e3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, results out
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h_in = [pin(t) for t in (x.q, x.k, x.v, x.do)]
+    for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
+        h.copy_(t)
+    outs = (step.o, step.lse, step.dq, step.dk, step.dv)
+    h_out = [pin(t) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    e2e_steps = max(1, min(args.steps, 3))
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
+            t.copy_(h, non_blocking=True)
+        step.run()
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = flops * world * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = None
+    if TRAFFIC["sha1"] and TRAFFIC["kernel_source"] and source_sha(TRAFFIC["kernel_source"]) == TRAFFIC["sha1"]:
+        traffic = TRAFFIC["bytes_per_launch"]
+    mbytes = merge_bytes(w, len(step.windows))
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "n_clean": w.n, "n_corrupted": w.n, "block": w.block, "heads": w.heads,
+                   "kv_heads": w.kv_heads, "head_dim": w.head_dim, "clean_shards": w.shards,
+                   "l2": "inputs larger than L2 (q alone 2.1 GB), no flush", "parallelism": f"replicas{world}"},
+        "roofline": {"kernel": "bdlm_attn_bwd (key-major main kernel + preprocess + dq convert)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained"},
+        "components": {
+            "fwd_partials_ms": fwd_ms, "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
+            "merge_ms": mrg_ms, "merge_gbs": mbytes / (mrg_ms / 1e3) / 1e9,
+            "merge_frac_hbm": mbytes / (mrg_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+            "bwd_ms": bwd_ms, "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,
+            "fwd_frac_bf16": f_fwd / (fwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
+            "bwd_frac_bf16": f_bwd / (bwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
+            "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xh = host_group0(x, w)
+        rate, pr, dt, nblk = oracle_sample(xh, w, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = {
+            "value": 14 * w.head_dim * rate / 1e12, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"float64 oracle fwd+bwd on {nblk} query blocks (B={w.block} rows, latest first) of kv "
+                      f"group 0 ({w.heads // w.kv_heads} q heads) of this workload, {pr} valid pairs in {dt:.1f} s",
+        }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("bench.py: at least 3 warm-up steps are required; using 3")
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_cuda(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

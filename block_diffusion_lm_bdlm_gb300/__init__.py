@@ -1,0 +1,235 @@
+"""GB300-native BDLM attention: Python binding of libbdlm.
+
+Argument marshalling only. Every step of the computation runs in the CUDA
+kernels of libbdlm.so (built in-tree from csrc/ for sm_103a); there is no
+Python or CPU fallback, and a missing library raises. PyTorch supplies device
+memory and the current stream.
+
+The C functions are declared in include/bdlm.h; the Python names are the same:
+  bdlm_attn_fwd(q, k, v, block, ...) -> (o, lse)
+  bdlm_attn_bwd(q, k, v, o, lse, dO, block, ...) -> (dq, dk, dv)
+  bdlm_lse_merge(partials, lses) -> (o, lse)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from .build import LIB
+
+__all__ = [
+    "BDLMError", "Partial", "bdlm_attn_fwd", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
+    "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_last_launch_count",
+    "load_library", "EXPORTED_SYMBOLS",
+]
+
+BDLM_OK = 0
+BDLM_BF16, BDLM_F32 = 0, 1
+PART_NONE, PART_KEY_WINDOW, PART_BLOCK_GROUP = 0, 1, 2
+
+EXPORTED_SYMBOLS = (
+    "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_attn_fwd", "bdlm_attn_bwd",
+    "bdlm_lse_merge", "bdlm_read_error", "bdlm_status_string", "bdlm_last_launch_count",
+)
+
+
+class BDLMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class _CPartial(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("n_q_blocks", ctypes.c_int32), ("key_lo", ctypes.c_int64),
+                ("key_hi", ctypes.c_int64), ("q_blocks", ctypes.c_void_p)]
+
+
+@dataclass
+class Partial:
+    """Restriction of a forward call (see bdlm_partial in include/bdlm.h).
+
+    Partial.window(lo, hi): k/v hold the keys at positions [lo, hi).
+    Partial.group(blocks): q holds the corrupted rows of `blocks` (device int32).
+    """
+    kind: int
+    key_lo: int = 0
+    key_hi: int = 0
+    q_blocks: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def window(lo: int, hi: int) -> "Partial":
+        return Partial(PART_KEY_WINDOW, key_lo=int(lo), key_hi=int(hi))
+
+    @staticmethod
+    def group(blocks: torch.Tensor) -> "Partial":
+        return Partial(PART_BLOCK_GROUP, q_blocks=blocks)
+
+    def c(self) -> _CPartial:
+        nb, ptr = 0, None
+        if self.kind == PART_BLOCK_GROUP:
+            b = self.q_blocks
+            if b is None or b.dtype != torch.int32 or not b.is_cuda or not b.is_contiguous():
+                raise ValueError("q_blocks must be a contiguous int32 CUDA tensor")
+            nb, ptr = b.numel(), b.data_ptr()
+        return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr)
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libbdlm.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(f"{LIB} is missing: build it with `python -m block_diffusion_lm_bdlm_gb300.build`")
+    lib = ctypes.CDLL(LIB)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.bdlm_attn_fwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
+    lib.bdlm_attn_fwd_workspace_bytes.restype = sz
+    lib.bdlm_attn_bwd_workspace_bytes.argtypes = [i64, i32, i32, i32]
+    lib.bdlm_attn_bwd_workspace_bytes.restype = sz
+    lib.bdlm_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, i32, f32,
+                                  ctypes.POINTER(_CPartial), vp, sz, vp]
+    lib.bdlm_attn_fwd.restype = ctypes.c_int
+    lib.bdlm_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, i32, f32,
+                                  ctypes.POINTER(_CPartial), vp, sz, vp]
+    lib.bdlm_attn_bwd.restype = ctypes.c_int
+    lib.bdlm_lse_merge.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i64, i32, i32, vp, vp, vp]
+    lib.bdlm_lse_merge.restype = ctypes.c_int
+    lib.bdlm_read_error.argtypes = [vp, vp]
+    lib.bdlm_read_error.restype = ctypes.c_int
+    lib.bdlm_status_string.argtypes = [ctypes.c_int]
+    lib.bdlm_status_string.restype = ctypes.c_char_p
+    lib.bdlm_last_launch_count.argtypes = []
+    lib.bdlm_last_launch_count.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().bdlm_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != BDLM_OK:
+        raise BDLMError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bf16_cuda(name, t):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None, 1
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor")
+    return cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
+
+
+def bdlm_attn_fwd_workspace_bytes(L: int, heads: int, head_dim: int, n_docs: int = 1) -> int:
+    return int(load_library().bdlm_attn_fwd_workspace_bytes(L, heads, head_dim, n_docs))
+
+
+def bdlm_attn_bwd_workspace_bytes(L: int, heads: int, head_dim: int, n_docs: int = 1) -> int:
+    return int(load_library().bdlm_attn_bwd_workspace_bytes(L, heads, head_dim, n_docs))
+
+
+def bdlm_last_launch_count() -> int:
+    return int(load_library().bdlm_last_launch_count())
+
+
+def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=None, softmax_scale: float = 0.0,
+                  part: Optional[Partial] = None, out=None, lse=None, workspace=None, stream=None):
+    """BDLM attention forward. q [Lq,H,d], k/v [Lk,Hk,d] bf16 CUDA tensors.
+    L defaults to q's rows (full attention, key window) and must be given as
+    2n for a block group. Returns (o [Lq,H,d] bf16, lse [H,Lq] fp32)."""
+    lib = load_library()
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(nm, t)
+    Lq, H, d = q.shape
+    Hk = k.shape[1]
+    L = Lq if L is None else int(L)
+    cu_ptr, n_docs = _cu(cu_seqlens)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, Lq), dtype=torch.float32, device=q.device)
+    ws_bytes = lib.bdlm_attn_fwd_workspace_bytes(L, H, d, n_docs)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    cpart = ctypes.byref(part.c()) if part is not None else None
+    st = lib.bdlm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L, block, H,
+                           Hk, d, cu_ptr, n_docs, softmax_scale, cpart, workspace.data_ptr(),
+                           workspace.numel(), _stream(stream))
+    _check(st, "bdlm_attn_fwd")
+    return out, lse
+
+
+def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, cu_seqlens=None, softmax_scale: float = 0.0,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """BDLM attention backward of the full forward. Returns (dq, dk, dv) bf16."""
+    lib = load_library()
+    for nm, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        _bf16_cuda(nm, t)
+    L, H, d = q.shape
+    Hk = k.shape[1]
+    cu_ptr, n_docs = _cu(cu_seqlens)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = lib.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.bdlm_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), L, block, H, Hk, d, cu_ptr, n_docs,
+                           softmax_scale, None, workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(st, "bdlm_attn_bwd")
+    return dq, dk, dv
+
+
+def bdlm_lse_merge(partials: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], *, out=None, lse=None,
+                   stream=None):
+    """Merge partials [rows,H,d] (bf16 or fp32) with their lse [H,rows]."""
+    lib = load_library()
+    P = len(partials)
+    if P == 0 or P != len(lses):
+        raise ValueError("need as many lse tensors as partials (at least one)")
+    rows, H, d = partials[0].shape
+    dt = partials[0].dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("partials must be bf16 or fp32")
+    for p, l in zip(partials, lses):
+        if p.shape != partials[0].shape or p.dtype != dt or not p.is_cuda or not p.is_contiguous():
+            raise ValueError("partials must share one shape and dtype and be contiguous CUDA tensors")
+        if l.shape != (H, rows) or l.dtype != torch.float32 or not l.is_cuda or not l.is_contiguous():
+            raise ValueError("each lse must be a contiguous fp32 CUDA tensor [H, rows]")
+    if out is None:
+        out = torch.empty((rows, H, d), dtype=torch.bfloat16, device=partials[0].device)
+    if lse is None:
+        lse = torch.empty((H, rows), dtype=torch.float32, device=partials[0].device)
+    pp = (ctypes.c_void_p * P)(*[p.data_ptr() for p in partials])
+    lp = (ctypes.c_void_p * P)(*[l.data_ptr() for l in lses])
+    st = lib.bdlm_lse_merge(pp, lp, P, BDLM_F32 if dt == torch.float32 else BDLM_BF16, rows, H, d,
+                            out.data_ptr(), lse.data_ptr(), _stream(stream))
+    _check(st, "bdlm_lse_merge")
+    return out, lse
+
+
+def bdlm_read_error(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device error word of the last call
+    that used `workspace` (0 = none)."""
+    return int(load_library().bdlm_read_error(workspace.data_ptr(), _stream(stream)))

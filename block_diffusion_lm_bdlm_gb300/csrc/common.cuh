@@ -1,0 +1,109 @@
+// common.cuh - layout decode shared by the BDLM kernels.
+//
+// Every query row of a call has at most two key intervals, in k-row
+// coordinates of the call's k/v buffers:
+//   prefix [p_lo, p_hi): the clean keys it sees (clean blocks <= b for a clean
+//                        row of block b, clean blocks < b for a corrupted row),
+//   diag   [d_lo, d_hi): its own corrupted block (corrupted rows only).
+// This is the BDLM mask of "Block Parallelism For Efficient Distributed
+// Long-Context Diffusion Language Model Training" (abstract) and the rit.work
+// CSBP post (first section), restated per row so that a tile of rows iterates
+// contiguous key ranges and only boundary tiles need an element mask.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bdlm {
+
+enum Mode : int { MODE_FULL = 0, MODE_WINDOW = 1, MODE_GROUP = 2 };
+
+// Status codes written to the device error word (same values as bdlm.h).
+enum DevStatus : int { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_CHECK = 6 };
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+    int error;     // first device error (0 = none)
+    int info;      // detail of the first error (e.g. offending document)
+    int n_tiles;   // tiles enumerated by the prologue
+    int counter;   // dynamic work counter of the main kernel
+    int counter2;  // second counter (second kernel of a call)
+    int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// How the rows of a call map to sequence positions.
+struct Layout {
+    int mode;
+    int B;             // diffusion block size
+    int n;             // clean length (single sequence / window / group)
+    int kw_lo, kw_hi;  // MODE_WINDOW: key positions held by k/v
+    const int* cu;     // MODE_FULL: device cu_seqlens, or nullptr for one sequence
+    int n_docs;
+    long long L;       // rows of the full concatenation
+    const int* blocks; // MODE_GROUP: device list of corrupted block ids
+    int n_blocks;
+};
+
+// One tile of consecutive rows that never straddles a document half.
+// q row of tile row r = doc_start + pos0 + r.
+struct Tile {
+    int doc_start;  // first row of the document (0 for window / group)
+    int n;          // clean length of the document
+    int pos0;       // document position (full/window) or list row (group) of row 0
+    int nrows;      // valid rows (<= tile height)
+};
+
+struct Span {
+    int p_lo, p_hi, d_lo, d_hi;
+};
+
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
+
+// Key intervals of tile row r (empty intervals are [0, 0)).
+__device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r) {
+    Span s{0, 0, 0, 0};
+    if (r >= t.nrows) return s;
+    const int B = lay.B;
+    if (lay.mode == MODE_GROUP) {
+        const int j = t.pos0 + r;
+        const int li = j / B;
+        const int b = __ldg(lay.blocks + li);
+        if (b > 0) { s.p_lo = 0; s.p_hi = b * B; }
+        s.d_lo = lay.n + li * B;
+        s.d_hi = s.d_lo + B;
+        return s;
+    }
+    const int n = t.n;
+    const int pos = t.pos0 + r;
+    const int kw_lo = lay.mode == MODE_WINDOW ? lay.kw_lo : 0;
+    const int kw_hi = lay.mode == MODE_WINDOW ? lay.kw_hi : 2 * n;
+    const int kbase = t.doc_start - kw_lo;
+    int pref_hi, dlo = 0, dhi = 0;
+    if (pos < n) {
+        pref_hi = (pos / B + 1) * B;
+    } else {
+        const int b = (pos - n) / B;
+        pref_hi = b * B;
+        dlo = n + b * B;
+        dhi = dlo + B;
+    }
+    int lo = imax(0, kw_lo), hi = imin(pref_hi, imin(kw_hi, n));
+    if (hi > lo) { s.p_lo = kbase + lo; s.p_hi = kbase + hi; }
+    lo = imax(dlo, kw_lo);
+    hi = imin(dhi, kw_hi);
+    if (dhi > dlo && hi > lo) { s.d_lo = kbase + lo; s.d_hi = kbase + hi; }
+    return s;
+}
+
+__device__ __forceinline__ bool span_sees(const Span& s, int kr) {
+    return (kr >= s.p_lo && kr < s.p_hi) || (kr >= s.d_lo && kr < s.d_hi);
+}
+
+__device__ __forceinline__ void set_error(WsHeader* h, int code, int info) {
+    if (atomicCAS(&h->error, 0, code) == 0) atomicExch(&h->info, info);
+}
+
+}  // namespace bdlm

@@ -1,0 +1,76 @@
+// kernels.h - internal launch interface between the C ABI and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace bdlm {
+
+// Workspace carve-up (all pointers inside the caller's workspace).
+struct WsCarve {
+    WsHeader* hdr;
+    Tile* table;    // ordered tiles
+    Tile* tmp;      // unordered tiles (prologue scratch)
+    int* cost;      // per-tile cost (prologue scratch)
+    int max_tiles;
+    float* D;       // backward: rowsum(dO * o), [H, L]
+    float* dqacc;   // backward: fp32 dq accumulator, [L, H, d]
+};
+
+struct FwdArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    __nv_bfloat16* o;
+    float* lse;
+    Layout lay;
+    int H, Hk, G, D;
+    float scale_log2;  // softmax scale * log2(e)
+    long long Lq, Lk;  // rows of q and of k
+    const Tile* table;
+    WsHeader* hdr;
+};
+
+struct BwdArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* o;
+    const float* lse;
+    const __nv_bfloat16* dO;
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    float* Dsum;
+    float* dqacc;
+    Layout lay;
+    int H, Hk, G, D;
+    float scale, scale_log2;
+    long long L;
+    const Tile* table;
+    WsHeader* hdr;
+};
+
+struct MergeArgs {
+    const void* part[64];
+    const float* lse_in[64];
+    int P;
+    int f32;  // partials are fp32
+    long long rows;
+    int H, D;
+    __nv_bfloat16* o;
+    float* lse;
+};
+
+// Tile heights used by the kernels (the prologue enumerates in these units).
+constexpr int kFwdTileRows = 64;
+constexpr int kFwdKeyTile = 64;
+constexpr int kBwdKeyTile = 64;
+constexpr int kBwdQTile = 64;
+
+void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, const WsCarve& ws,
+                      cudaStream_t st);
+cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t st, int* launches);
+cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t st, int* launches);
+cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st, int* launches);
+
+}  // namespace bdlm

@@ -1,0 +1,226 @@
+// sched.cu - tile enumeration and ordering for the BDLM kernels.
+//
+// One small kernel, launched before every attention kernel, that
+//   1. clears the workspace header (error word, work counters);
+//   2. validates cu_seqlens / the block list on the device;
+//   3. enumerates the row tiles of the call (never straddling a document half)
+//      with a cost estimate in key tiles (forward) or query rows (backward);
+//   4. orders them by descending cost with a counting sort.
+// The attention kernels then take work items from the front of this list with
+// an atomic counter. Taking the heaviest remaining tile first is the
+// work-conserving form of pairing early and late blocks for balance (rit.work
+// CSBP post: the valid pairs are unchanged and early and late blocks are
+// assigned together): the last blocks of a sequence carry the longest clean
+// prefixes and are dealt first, the first blocks fill in behind them.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bdlm {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kBuckets = 8192;
+
+__device__ int block_exclusive_scan(int x, int* total, int* sbuf) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int v = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) sbuf[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = sbuf[lane];
+        int ws = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, ws, o);
+            if (lane >= o) ws += y;
+        }
+        sbuf[32 + lane] = ws - w;
+        if (lane == 31) sbuf[64] = ws;
+    }
+    __syncthreads();
+    int res = v - x + sbuf[32 + warp];
+    *total = sbuf[64];
+    __syncthreads();
+    return res;
+}
+
+__device__ void doc_of(const Layout& lay, int d, int* start, int* n) {
+    if (lay.mode == MODE_FULL && lay.cu) {
+        int s = __ldg(lay.cu + d), e = __ldg(lay.cu + d + 1);
+        *start = s;
+        *n = (e - s) / 2;
+    } else {
+        *start = 0;
+        *n = lay.n;
+    }
+}
+
+// Cost of a forward query tile, in key tiles of kn rows.
+__device__ int fwd_cost(const Layout& lay, const Tile& t, int kn) {
+    int len = 0;
+    if (lay.mode == MODE_GROUP) {
+        int b0 = t.pos0 / lay.B, b1 = (t.pos0 + t.nrows - 1) / lay.B;
+        int bmax = 0;
+        for (int i = b0; i <= b1; ++i) bmax = imax(bmax, __ldg(lay.blocks + i));
+        len = (bmax * lay.B + kn - 1) / kn + (t.nrows + lay.B + kn - 1) / kn;
+        return len;
+    }
+    Span a = row_span(lay, t, 0), z = row_span(lay, t, t.nrows - 1);
+    int p_lo = a.p_hi > a.p_lo ? a.p_lo : z.p_lo;
+    int p = z.p_hi > z.p_lo ? (z.p_hi - p_lo + kn - 1) / kn : 0;
+    int d_lo = a.d_hi > a.d_lo ? a.d_lo : z.d_lo;
+    int dd = z.d_hi > z.d_lo ? (z.d_hi - d_lo + kn - 1) / kn : 0;
+    return p + dd;
+}
+
+// Cost of a backward key tile, in query rows that see it.
+__device__ int bwd_cost(const Layout& lay, const Tile& t) {
+    const int n = t.n, B = lay.B;
+    if (t.pos0 < n) {
+        int b = t.pos0 / B;
+        return (n - b * B) + imax(0, n - (b + 1) * B);
+    }
+    int b0 = (t.pos0 - n) / B, b1 = (t.pos0 + t.nrows - 1 - n) / B;
+    return (b1 - b0 + 1) * B;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table, Tile* tmp,
+                 int* cost_tmp, WsHeader* hdr, int max_tiles, int cost_shift) {
+    __shared__ int hist[kBuckets];
+    __shared__ int sbuf[96];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        hdr->error = 0;
+        hdr->info = 0;
+        hdr->n_tiles = 0;
+        hdr->counter = 0;
+        hdr->counter2 = 0;
+        s_carry = 0;
+    }
+    for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
+
+    // ---- device-side validation -------------------------------------------
+    int bad = 0, bad_info = 0;
+    const int ndocs = (lay.mode == MODE_FULL && lay.cu) ? lay.n_docs : 1;
+    if (lay.mode == MODE_FULL && lay.cu) {
+        for (int d = tid; d < ndocs; d += kThreads) {
+            long long s = __ldg(lay.cu + d), e = __ldg(lay.cu + d + 1);
+            long long len = e - s;
+            if (len <= 0 || (len & 1) || ((len / 2) % lay.B) != 0) { bad = 1; bad_info = d; }
+        }
+        if (tid == 0 && (__ldg(lay.cu) != 0 || (long long)__ldg(lay.cu + ndocs) != lay.L)) {
+            bad = 1;
+            bad_info = -1;
+        }
+    }
+    if (lay.mode == MODE_GROUP) {
+        const int nb = lay.n / lay.B;
+        for (int i = tid; i < lay.n_blocks; i += kThreads) {
+            int b = __ldg(lay.blocks + i);
+            if (b < 0 || b >= nb) { bad = 1; bad_info = i; }
+        }
+    }
+    if (__syncthreads_or(bad)) {
+        if (bad) set_error(hdr, DEV_CHECK, bad_info);
+        return;
+    }
+
+    // ---- enumeration ---------------------------------------------------------
+    if (lay.mode == MODE_GROUP) {
+        const int rows = lay.n_blocks * lay.B;
+        const int nt = (rows + tile_rows - 1) / tile_rows;
+        for (int i = tid; i < nt; i += kThreads) {
+            Tile t{0, lay.n, i * tile_rows, imin(tile_rows, rows - i * tile_rows)};
+            int c = fwd_cost(lay, t, key_tile) >> cost_shift;
+            c = imin(c, kBuckets - 1);
+            tmp[i] = t;
+            cost_tmp[i] = c;
+            atomicAdd(&hist[c], 1);
+        }
+        if (tid == 0) s_carry = nt;
+        __syncthreads();
+    } else {
+        for (int base = 0; base < ndocs; base += kThreads) {
+            const int d = base + tid;
+            int start = 0, n = 0, per_half = 0;
+            if (d < ndocs) {
+                doc_of(lay, d, &start, &n);
+                per_half = (n + tile_rows - 1) / tile_rows;
+            }
+            int total;
+            int off = block_exclusive_scan(2 * per_half, &total, sbuf);
+            const int carry = s_carry;
+            if (d < ndocs) {
+                for (int i = 0; i < 2 * per_half; ++i) {
+                    const int half = i / per_half, j = i % per_half;
+                    const int p0 = half * n + j * tile_rows;
+                    Tile t{start, n, p0, imin(tile_rows, (half + 1) * n - p0)};
+                    int c = kind == 0 ? fwd_cost(lay, t, key_tile) : bwd_cost(lay, t);
+                    c = imin(c >> cost_shift, kBuckets - 1);
+                    const int idx = carry + off + i;
+                    if (idx < max_tiles) {
+                        tmp[idx] = t;
+                        cost_tmp[idx] = c;
+                        atomicAdd(&hist[c], 1);
+                    }
+                }
+            }
+            __syncthreads();
+            if (tid == 0) s_carry = carry + total;
+            __syncthreads();
+        }
+    }
+    const int n_tiles = s_carry;
+    if (n_tiles > max_tiles) {
+        if (tid == 0) set_error(hdr, DEV_CHECK, -2);
+        return;
+    }
+    __syncthreads();
+
+    // ---- counting sort, heaviest first ----------------------------------------
+    // bucket c starts after all buckets c' > c
+    constexpr int per = kBuckets / kThreads;
+    const int first = kBuckets - (tid + 1) * per;  // thread 0 owns the top buckets
+    int local = 0;
+    for (int i = 0; i < per; ++i) local += hist[first + i];
+    int total;
+    int off = block_exclusive_scan(local, &total, sbuf);
+    __syncthreads();
+    {
+        int run = off;
+        for (int i = per - 1; i >= 0; --i) {
+            int c = hist[first + i];
+            hist[first + i] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < n_tiles; i += kThreads) {
+        int pos = atomicAdd(&hist[cost_tmp[i]], 1);
+        table[pos] = tmp[i];
+    }
+    if (tid == 0) hdr->n_tiles = n_tiles;
+}
+
+}  // namespace
+
+void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, const WsCarve& ws,
+                      cudaStream_t st) {
+    // keep the costs inside the histogram for very long sequences
+    int shift = 0;
+    long long max_cost = kind == 0 ? (2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n)) / key_tile + 4
+                                   : 2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n);
+    while ((max_cost >> shift) >= kBuckets) ++shift;
+    enumerate_kernel<<<1, kThreads, 0, st>>>(lay, tile_rows, key_tile, kind, ws.table, ws.tmp,
+                                             ws.cost, ws.hdr, ws.max_tiles, shift);
+}
+
+}  // namespace bdlm

@@ -1,0 +1,172 @@
+/*
+ * bdlm.h - C ABI of the GB300 (sm_103a) BDLM attention library.
+ *
+ * The library computes core attention softmax(QK^T)V ("Efficient Long-context
+ * Language Model Training by Core Attention Disaggregation", abstract), its
+ * backward, and the log-sum-exp merge of partial results, under the mask of
+ * block diffusion LM training ("Block Parallelism For Efficient Distributed
+ * Long-Context Diffusion Language Model Training", abstract; rit.work CSBP
+ * post, first section):
+ *
+ *   each sequence is [clean n rows | corrupted n rows], cut into blocks of B;
+ *   a clean row of block b sees the clean rows of blocks <= b;
+ *   a corrupted row of block b sees the clean rows of blocks < b and every
+ *   corrupted row of its own block b; clean rows never see corrupted rows.
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense, row-major, 16-byte aligned device buffers:
+ *       q, o, dO, dq : bf16 [Lq, H, d]       k, v, dk, dv : bf16 [Lk, Hk, d]
+ *       lse          : fp32 [H, Lq]          (natural log of sum_j exp(scale*q.k_j))
+ *   - Query head h reads kv head h / (H / Hk).
+ *   - d is 64 or 128; H % Hk == 0; 1 <= B <= 1024; every document's clean
+ *     length is a positive multiple of B.
+ *   - The caller owns every buffer, including the workspace. The library never
+ *     allocates or frees device memory and never synchronises, except in
+ *     bdlm_read_error. Every call is asynchronous on `stream` (NULL = the
+ *     legacy default stream) and runs on the current CUDA device.
+ *   - Arguments that can be checked on the host are checked before any launch;
+ *     on failure the call returns a status and launches nothing. Problems found
+ *     on the device (a malformed cu_seqlens, a wait that timed out) are written
+ *     to an error word inside the workspace, read with bdlm_read_error.
+ *   - Not thread-safe per workspace: two calls that share a workspace must be
+ *     ordered on one stream.
+ */
+#ifndef BDLM_H
+#define BDLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BDLM_API __attribute__((visibility("default")))
+#else
+#define BDLM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bdlm_stream_t; /* the same type as cudaStream_t */
+
+enum bdlm_status {
+    BDLM_OK = 0,
+    BDLM_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer       */
+    BDLM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d = 96)         */
+    BDLM_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required      */
+    BDLM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed               */
+    BDLM_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out                  */
+    BDLM_ERR_DEVICE_CHECK = 6  /* device: cu_seqlens or block list is malformed   */
+};
+
+enum bdlm_dtype { BDLM_BF16 = 0, BDLM_F32 = 1 };
+
+enum bdlm_part_kind {
+    BDLM_PART_NONE = 0,        /* full BDLM attention                             */
+    BDLM_PART_KEY_WINDOW = 1,  /* keys restricted to one contiguous window        */
+    BDLM_PART_BLOCK_GROUP = 2  /* queries restricted to a list of corrupted blocks*/
+};
+
+/*
+ * Restriction of one forward call (single sequence only; cu_seqlens == NULL).
+ *
+ * BDLM_PART_KEY_WINDOW - partial attention against one shard of the keys, as
+ *   each rank computes it under context-sharded block parallelism (Block
+ *   Parallelism abstract; rit.work CSBP post, CSBP paragraph). k and v hold
+ *   exactly the keys at sequence positions [key_lo, key_hi) (Lk = key_hi -
+ *   key_lo rows); q holds all L rows. A clean shard is a window inside [0, n);
+ *   the local corrupted keys are the window [n, 2n). Query rows with no visible
+ *   key in the window get o = 0 and lse = -inf.
+ *
+ * BDLM_PART_BLOCK_GROUP - the corrupted target blocks owned by one rank under
+ *   block parallelism (rit.work CSBP post, block-parallelism paragraph). q
+ *   holds the corrupted rows of the listed blocks, B rows each, in list order
+ *   (Lq = n_q_blocks * B). k and v hold the n clean rows followed by the same
+ *   blocks' corrupted rows in the same order (Lk = n + n_q_blocks * B).
+ *   q_blocks is a DEVICE array of distinct block ids in [0, n / B).
+ */
+typedef struct {
+    int32_t kind;            /* enum bdlm_part_kind                               */
+    int32_t n_q_blocks;      /* BLOCK_GROUP: number of listed blocks              */
+    int64_t key_lo, key_hi;  /* KEY_WINDOW: sequence positions, 0<=lo<hi<=L       */
+    const int32_t* q_blocks; /* BLOCK_GROUP: device int32 [n_q_blocks]            */
+} bdlm_partial;
+
+/* Workspace sizes (bytes) for one call with L query rows, H heads, head dim d
+ * and n_docs packed documents (1 for a single sequence). Returns 0 for sizes
+ * the library does not support. The workspace must be 256-byte aligned. */
+BDLM_API size_t bdlm_attn_fwd_workspace_bytes(int64_t L, int32_t heads, int32_t head_dim, int32_t n_docs);
+BDLM_API size_t bdlm_attn_bwd_workspace_bytes(int64_t L, int32_t heads, int32_t head_dim, int32_t n_docs);
+
+/*
+ * Forward: o = softmax(scale * q k^T under the BDLM mask) v, lse per row.
+ *
+ *   L          rows of the full concatenation: 2n for one sequence, or
+ *              cu_seqlens[n_docs] for packed documents (each document is
+ *              [clean n_d | corrupted n_d]). With BLOCK_GROUP, L = 2n still
+ *              names the sequence and q holds only the group's rows.
+ *   block      B, the diffusion block size.
+ *   cu_seqlens NULL for one sequence, else a DEVICE int32 [n_docs + 1] of
+ *              document offsets (0, ..., L); checked on the device
+ *              (BDLM_ERR_DEVICE_CHECK through bdlm_read_error).
+ *   softmax_scale  <= 0 selects 1/sqrt(d).
+ *   part       NULL or kind NONE for full attention; see bdlm_partial.
+ *   workspace  >= bdlm_attn_fwd_workspace_bytes(L, heads, head_dim, n_docs).
+ * Writes o [Lq, H, d] bf16 and lse [H, Lq] fp32.
+ */
+BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                  const int32_t* cu_seqlens, int32_t n_docs, float softmax_scale,
+                  const bdlm_partial* part, void* workspace, size_t workspace_bytes,
+                  bdlm_stream_t stream);
+
+/*
+ * Backward of the full forward (part must be NULL or kind NONE): given q, k, v,
+ * the forward's o and lse, and the upstream gradient dO, writes
+ * dq [L, H, d], dk [L, Hk, d], dv [L, Hk, d] (bf16). dk and dv sum the
+ * contributions of all H/Hk query heads that share a kv head. The workspace
+ * (>= bdlm_attn_bwd_workspace_bytes) holds D = rowsum(dO * o) and an fp32 dq
+ * accumulator; its contents need no initialisation.
+ */
+BDLM_API int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv,
+                  int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                  const int32_t* cu_seqlens, int32_t n_docs, float softmax_scale,
+                  const bdlm_partial* part, void* workspace, size_t workspace_bytes,
+                  bdlm_stream_t stream);
+
+/*
+ * LSE merge of n_partials results computed against disjoint key sets (the
+ * per-shard combination under context-sharded block parallelism):
+ *   m = max_p lse_p over finite values, w_p = exp(lse_p - m) (0 for -inf),
+ *   lse = m + ln sum_p w_p,  o = sum_p w_p o_p / sum_p w_p.
+ * A row whose partials are all -inf gets o = 0, lse = -inf; a -inf partial is
+ * skipped by selection, so whatever its o_p holds never reaches the output.
+ *
+ *   partials   HOST array of n_partials DEVICE pointers, each [rows, H, d] of
+ *              partial_dtype (BDLM_BF16 or BDLM_F32).
+ *   lses       HOST array of n_partials DEVICE pointers, each fp32 [H, rows].
+ *   o, lse     outputs: bf16 [rows, H, d], fp32 [H, rows]; may not alias inputs.
+ *   1 <= n_partials <= 64; d is 64 or 128.
+ */
+BDLM_API int bdlm_lse_merge(const void* const* partials, const float* const* lses, int32_t n_partials,
+                   int32_t partial_dtype, int64_t rows, int32_t heads, int32_t head_dim,
+                   void* o, float* lse, bdlm_stream_t stream);
+
+/* Synchronises `stream`, then returns the device error word of the last call
+ * that used `workspace` (BDLM_OK, BDLM_ERR_TIMEOUT or BDLM_ERR_DEVICE_CHECK),
+ * or BDLM_ERR_CUDA if the stream reports a CUDA error. */
+BDLM_API int bdlm_read_error(const void* workspace, bdlm_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+BDLM_API const char* bdlm_status_string(int status);
+
+/* Number of kernels the last successful bdlm_* call on this host thread
+ * launched (for launch accounting in benchmarks). */
+BDLM_API int bdlm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BDLM_H */

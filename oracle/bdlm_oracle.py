@@ -143,17 +143,19 @@ def bdlm_attention(q, k, v, block, scale, cu_seqlens=None, do=None,
     [clean n | corrupted n]. `row_blocks`, if given, is a list of
     (doc index, doc-local first row) of the query blocks to compute; o, lse, dq
     are then valid on those rows only and dk/dv hold only their contributions.
-    Returns dict with o, lse and (with do) dq, dk, dv.
+    Inputs may be float32 arrays holding bf16 values (to save host memory at
+    long lengths): every gathered block is converted to float64 before any
+    arithmetic. Returns dict with o, lse and (with do) dq, dk, dv (float64).
     """
     L, H, d = q.shape
     docs = _docs(L, cu_seqlens)
-    o = np.zeros_like(q)
+    o = np.zeros(q.shape)
     lse = np.full((H, L), NEG_INF)
     grads = do is not None
     if grads:
-        dq = np.zeros_like(q)
-        dk = np.zeros_like(k)
-        dv = np.zeros_like(v)
+        dq = np.zeros(q.shape)
+        dk = np.zeros(k.shape)
+        dv = np.zeros(v.shape)
     if row_blocks is None:
         work = []
         for di, (s0, ln) in enumerate(docs):
@@ -168,12 +170,13 @@ def bdlm_attention(q, k, v, block, scale, cu_seqlens=None, do=None,
         mrow = mask_rows(rows, n, block)
         cols = np.nonzero(mrow.any(axis=0))[0]
         sub = mrow[:, cols]
-        qa, ka, va = q[s0 + rows], k[s0 + cols], v[s0 + cols]
+        f64 = lambda x: np.asarray(x, dtype=np.float64)
+        qa, ka, va = f64(q[s0 + rows]), f64(k[s0 + cols]), f64(v[s0 + cols])
         ob, lb = attend(qa, ka, va, sub, scale)
         o[s0 + rows] = ob
         lse[:, s0 + rows] = lb
         if grads:
-            dqb, dkb, dvb = attend_bwd(qa, ka, va, sub, scale, ob, lb, do[s0 + rows])
+            dqb, dkb, dvb = attend_bwd(qa, ka, va, sub, scale, ob, lb, f64(do[s0 + rows]))
             dq[s0 + rows] = dqb
             if want_kv_grads:
                 np.add.at(dk, s0 + cols, dkb)

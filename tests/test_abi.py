@@ -1,0 +1,131 @@
+"""Host-side tests of the C ABI: the library builds for sm_103a, loads, exports
+every function include/bdlm.h declares, and rejects bad arguments before any
+launch. No compute call is made (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_diffusion_lm_bdlm_gb300 import build
+
+    build.build()
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    return bd.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "bdlm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bdlm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for f in ("bdlm_attn_fwd", "bdlm_attn_bwd", "bdlm_lse_merge"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    names = declared_functions()
+    assert set(names) == set(bd.EXPORTED_SYMBOLS)
+    for f in names:
+        assert hasattr(lib, f), f
+
+
+def test_library_is_built_for_sm103a():
+    from block_diffusion_lm_bdlm_gb300 import build
+
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+    assert os.path.exists(build.LIB)
+
+
+def test_status_strings(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    assert bd.status_string(0) == "BDLM_OK"
+    assert bd.status_string(5) == "BDLM_ERR_TIMEOUT"
+    assert bd.status_string(99) == "BDLM_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    f = lib.bdlm_attn_fwd_workspace_bytes
+    b = lib.bdlm_attn_bwd_workspace_bytes
+    assert f(1024, 4, 128, 1) >= 256
+    assert f(0, 4, 128, 1) == 0
+    assert f(1024, 4, 96, 1) == 0
+    L, H, d = 262144, 32, 128
+    # the backward keeps D [H, L] and an fp32 dq accumulator [L, H, d]
+    assert b(L, H, d, 1) - f(L, H, d, 1) >= L * H * 4 + L * H * d * 4
+
+
+def _fwd(lib, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=16, L=256, block=16, heads=2, kv_heads=2, head_dim=64, cu=None,
+                n_docs=1, scale=0.0, part=None, ws=256, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.bdlm_attn_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["L"], args["block"],
+                             args["heads"], args["kv_heads"], args["head_dim"], args["cu"], args["n_docs"],
+                             args["scale"], args["part"], args["ws"], args["ws_bytes"], args["stream"])
+
+
+def test_forward_rejects_bad_arguments(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    INVALID, UNSUP, WS = 1, 2, 3
+    assert _fwd(lib, q=None) == INVALID
+    assert _fwd(lib, k=17) == INVALID            # misaligned
+    assert _fwd(lib, L=255) == INVALID           # odd total length
+    assert _fwd(lib, L=200) == INVALID           # n = 100 not a multiple of 16
+    assert _fwd(lib, heads=3, kv_heads=2) == INVALID
+    assert _fwd(lib, head_dim=96) == UNSUP
+    assert _fwd(lib, ws=None) == WS
+    assert _fwd(lib, ws=272) == WS               # not 256-aligned
+    assert _fwd(lib, ws_bytes=16) == WS
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 10, 5, None)  # hi <= lo
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 0, 0, 0, None)  # no block list
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID
+    p = bd._CPartial(7, 0, 0, 0, None)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None)
+    assert _fwd(lib, part=ctypes.byref(p), cu=256, n_docs=1) == UNSUP  # windows need one sequence
+    assert lib.bdlm_last_launch_count() == 0
+
+
+def test_backward_and_merge_reject_bad_arguments(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None)
+    st = lib.bdlm_attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, 16, 2, 2, 64, None, 1, 0.0,
+                           ctypes.byref(p), 256, 1 << 20, None)
+    assert st == 2
+    st = lib.bdlm_attn_bwd(16, 16, 16, 16, 16, None, 16, 16, 16, 256, 16, 2, 2, 64, None, 1, 0.0, None, 256,
+                           1 << 20, None)
+    assert st == 1
+    VP = ctypes.c_void_p
+    parts = (VP * 2)(16, 32)
+    lses = (VP * 2)(64, 128)
+    assert lib.bdlm_lse_merge(parts, lses, 0, 0, 10, 2, 64, 256, 512, None) == 1      # no partials
+    assert lib.bdlm_lse_merge(parts, lses, 65, 0, 10, 2, 64, 256, 512, None) == 1     # too many
+    assert lib.bdlm_lse_merge(parts, lses, 2, 0, 10, 2, 96, 256, 512, None) == 2      # d = 96
+    assert lib.bdlm_lse_merge(parts, lses, 2, 3, 10, 2, 64, 256, 512, None) == 1      # dtype
+    assert lib.bdlm_lse_merge(parts, lses, 2, 0, 10, 2, 64, 16, 512, None) == 1       # o aliases a partial
+    bad = (VP * 2)(16, 33)
+    assert lib.bdlm_lse_merge(bad, lses, 2, 0, 10, 2, 64, 256, 512, None) == 1        # misaligned partial
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    q = torch.zeros(64, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        bd.bdlm_attn_fwd(q, q, q, 16)

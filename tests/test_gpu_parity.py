@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds that still
+span several tiles, ragged tails and the degenerate cases of the mask."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import check_grad, check_lse, check_o, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bd():
+    import block_diffusion_lm_bdlm_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def gen(n, block, H, Hk, d, seed, std=0.5, L=None):
+    w = synth.Workload("case", n=n, block=block, heads=H, kv_heads=Hk, head_dim=d, seed=seed, qkv_std=std)
+    return w, synth.make_inputs(w, device="cuda", rows=L)
+
+
+def ref_full(x, w, cu=None, heads=None):
+    q, k, v, do = host(x.q), host(x.k), host(x.v), host(x.do)
+    if heads is not None:
+        g0, g1 = heads
+        G = w.heads // w.kv_heads
+        q, do = q[:, g0 * G:g1 * G], do[:, g0 * G:g1 * G]
+        k, v = k[:, g0:g1], v[:, g0:g1]
+    return oracle.bdlm_attention(q, k, v, w.block, w.scale, cu_seqlens=cu, do=do)
+
+
+SHAPES = [
+    # n, block, H, Hk, d
+    (256, 16, 2, 2, 64),     # the tiny workload's shape
+    (96, 16, 4, 1, 128),     # ragged 64-row tiles, GQA 4:1
+    (128, 1, 2, 2, 64),      # block = 1: clean half is token-causal
+    (128, 128, 2, 1, 128),   # a single block
+    (320, 32, 8, 2, 128),    # several tiles per half
+    (200, 8, 3, 3, 64),      # odd head count, ragged
+    (64, 64, 1, 1, 128),     # one tile of one block
+]
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d", SHAPES)
+def test_full_forward_backward(bd, n, block, H, Hk, d):
+    w, x = gen(n, block, H, Hk, d, seed=n + block)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block)
+    torch.cuda.synchronize()
+    r = ref_full(x, w)
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
+
+
+def test_tiny_workload_sharded_and_merged(bd):
+    w = synth.WORKLOADS[0]
+    x = synth.make_inputs(w, device="cuda", keep_fp32=True)
+    n = w.n
+    r = ref_full(x, w)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, w.block)
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+    parts, lses = [], []
+    q64, k64, v64 = host(x.q), host(x.k), host(x.v)
+    for lo, hi in windows:
+        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), w.block,
+                                  part=bd.Partial.window(lo, hi))
+        pr = oracle.partial_attention(q64, k64[lo:hi], v64[lo:hi], n, w.block, lo, hi, w.scale)
+        check_o(host(po), pr["o"], f"partial[{lo},{hi}) o")
+        check_lse(host(pl), pr["lse"], f"partial[{lo},{hi}) lse")
+        parts.append(po)
+        lses.append(pl)
+    mo, ml = bd.bdlm_lse_merge(parts, lses)
+    torch.cuda.synchronize()
+    check_o(host(mo), r["o"], "merged o")
+    check_lse(host(ml), r["lse"], "merged lse")
+
+
+def test_merge_f32_partials_from_oracle(bd):
+    # the merge alone, fed the oracle's own partials (uploaded as fp32)
+    n, block, H, Hk, d = 192, 16, 4, 2, 128
+    w, x = gen(n, block, H, Hk, d, seed=5)
+    q64, k64, v64 = host(x.q), host(x.k), host(x.v)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale)
+    windows = synth.shard_bounds(n, 3) + [(n, 2 * n)]
+    parts, lses = [], []
+    for lo, hi in windows:
+        pr = oracle.partial_attention(q64, k64[lo:hi], v64[lo:hi], n, block, lo, hi, w.scale)
+        parts.append(torch.from_numpy(pr["o"]).float().cuda())
+        lses.append(torch.from_numpy(pr["lse"]).float().cuda())
+    mo, ml = bd.bdlm_lse_merge(parts, lses)
+    torch.cuda.synchronize()
+    check_o(host(mo), full["o"])
+    check_lse(host(ml), full["lse"])
+
+
+def test_merge_edge_cases(bd):
+    rows, H, d = 37, 2, 64
+    g = torch.Generator(device="cuda").manual_seed(3)
+    o1 = torch.randn(rows, H, d, device="cuda", generator=g).to(torch.bfloat16)
+    l1 = torch.randn(H, rows, device="cuda", generator=g)
+    junk = torch.full((rows, H, d), float("nan"), device="cuda").to(torch.bfloat16)
+    ninf = torch.full((H, rows), float("-inf"), device="cuda")
+    # single partial: identity
+    mo, ml = bd.bdlm_lse_merge([o1], [l1])
+    assert torch.equal(mo, o1)
+    assert torch.allclose(ml, l1, atol=1e-6)
+    # a -inf partial holding NaN is dropped
+    mo, ml = bd.bdlm_lse_merge([junk, o1], [ninf, l1])
+    assert torch.equal(mo, o1)
+    assert torch.allclose(ml, l1, atol=1e-6)
+    # all -inf: zeros and -inf
+    mo, ml = bd.bdlm_lse_merge([junk, junk], [ninf, ninf])
+    assert torch.all(mo == 0) and torch.all(torch.isneginf(ml))
+    # equal lse: average, lse + ln 2
+    o2 = torch.randn(rows, H, d, device="cuda", generator=g).to(torch.bfloat16)
+    mo, ml = bd.bdlm_lse_merge([o1, o2], [l1, l1])
+    torch.cuda.synchronize()
+    ref = (o1.float() + o2.float()) / 2
+    assert (mo.float() - ref).abs().max().item() <= 1e-2
+    assert torch.allclose(ml, l1 + math.log(2.0), atol=1e-5)
+
+
+def test_window_rows_without_keys(bd):
+    n, block, H, Hk, d = 256, 32, 2, 1, 128
+    w, x = gen(n, block, H, Hk, d, seed=9)
+    lo, hi = 192, 256  # a late clean shard: early clean and corrupted rows see nothing of it
+    po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), block,
+                              part=bd.Partial.window(lo, hi))
+    torch.cuda.synchronize()
+    pr = oracle.partial_attention(host(x.q), host(x.k)[lo:hi], host(x.v)[lo:hi], n, block, lo, hi, w.scale)
+    assert np.isneginf(pr["lse"]).sum() > 0
+    check_lse(host(pl), pr["lse"])
+    check_o(host(po), pr["o"])
+    empty = np.isneginf(pr["lse"]).T
+    assert np.all(host(po)[empty] == 0.0)
+
+
+@pytest.mark.parametrize("n,block,H,Hk,groups", [(512, 16, 4, 2, 4), (384, 32, 2, 1, 3)])
+def test_block_groups(bd, n, block, H, Hk, groups):
+    d = 128
+    w, x = gen(n, block, H, Hk, d, seed=11)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    q64, k64, v64 = host(x.q), host(x.k), host(x.v)
+    for blocks in synth.early_late_groups(n // block, groups):
+        qpos, kpos = oracle.group_positions(n, block, blocks)
+        qi = torch.from_numpy(qpos).cuda()
+        ki = torch.from_numpy(kpos).cuda()
+        bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
+        go, gl = bd.bdlm_attn_fwd(x.q[qi].contiguous(), x.k[ki].contiguous(), x.v[ki].contiguous(), block,
+                                  L=2 * n, part=bd.Partial.group(bl))
+        torch.cuda.synchronize()
+        r = oracle.group_attention(q64[qpos], k64[kpos], v64[kpos], n, block, blocks, w.scale)
+        check_o(host(go), r["o"], "group o")
+        check_lse(host(gl), r["lse"], "group lse")
+        # equal to the unsplit call on the same rows
+        assert (go.float() - o[qi].float()).abs().max().item() <= 2e-2
+        assert (gl - lse[:, qi]).abs().max().item() <= 1e-3 * max(1.0, lse.abs().max().item())
+
+
+def test_packed_documents(bd):
+    block, H, Hk, d = 32, 4, 2, 128
+    lens = [128, 64, 320, 192, 64]
+    cu = synth.cu_seqlens_of(lens)
+    g = torch.Generator(device="cuda").manual_seed(13)
+    T = cu[-1]
+    mk = lambda *s: (torch.randn(*s, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    q, k, v = mk(T, H, d), mk(T, Hk, d), mk(T, Hk, d)
+    do = (torch.randn(T, H, d, device="cuda", generator=g)).to(torch.bfloat16)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o, lse = bd.bdlm_attn_fwd(q, k, v, block, cu_seqlens=cu_d)
+    dq, dk, dv = bd.bdlm_attn_bwd(q, k, v, o, lse, do, block, cu_seqlens=cu_d)
+    torch.cuda.synchronize()
+    r = oracle.bdlm_attention(host(q), host(k), host(v), block, 1 / math.sqrt(d), cu_seqlens=cu, do=host(do))
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
+
+
+def test_zero_keys_closed_form(bd):
+    n, block, H, d = 192, 16, 2, 128
+    w, x = gen(n, block, H, H, d, seed=17)
+    k = torch.zeros_like(x.k)
+    o, lse = bd.bdlm_attn_fwd(x.q, k, x.v, block)
+    torch.cuda.synchronize()
+    lse_h = host(lse)
+    v = host(x.v)
+    o_h = host(o)
+    for i in range(2 * n):
+        b = (i % n) // block
+        assert np.all(np.abs(lse_h[:, i] - math.log((b + 1) * block)) <= 1e-5 * math.log((b + 1) * block) + 1e-6)
+        vis = np.arange(0, (b + 1) * block) if i < n else np.concatenate(
+            [np.arange(0, b * block), n + b * block + np.arange(block)])
+        assert np.abs(o_h[i] - v[vis].mean(axis=0)).max() <= 8e-3
+
+
+def test_malformed_cu_seqlens_is_reported(bd):
+    block, H, d = 32, 2, 64
+    T = 256
+    q = torch.zeros(T, H, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(T, H, d, 2), dtype=torch.uint8, device="cuda")
+    for bad in ([0, 63, 256], [0, 96, 256], [0, 128, 200]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        bd.bdlm_attn_fwd(q, q, q, block, cu_seqlens=cu, workspace=ws)
+        assert bd.bdlm_read_error(ws) == 6, bad
+    cu = torch.tensor([0, 128, 256], dtype=torch.int32, device="cuda")
+    bd.bdlm_attn_fwd(q, q, q, block, cu_seqlens=cu, workspace=ws)
+    assert bd.bdlm_read_error(ws) == 0
+
+
+def test_forward_is_deterministic(bd):
+    w, x = gen(512, 32, 4, 2, 128, seed=19)
+    o1, l1 = bd.bdlm_attn_fwd(x.q, x.k, x.v, 32)
+    o2, l2 = bd.bdlm_attn_fwd(x.q, x.k, x.v, 32)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_mid_workload(bd):
+    """8192 + 8192 rows, 32/8 heads, B = 32: one kv group in full (o, lse, all
+    gradients) and 8 sampled query blocks on every head (o, lse, dq)."""
+    w = synth.WORKLOADS[1]
+    x = synth.make_inputs(w, device="cuda")
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, w.block)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, w.block)
+    torch.cuda.synchronize()
+    G = w.heads // w.kv_heads
+    r = ref_full(x, w, heads=(0, 1))
+    check_o(host(o[:, :G]), r["o"])
+    check_lse(host(lse[:G]), r["lse"])
+    check_grad(host(dq[:, :G]), r["dq"], "dq")
+    check_grad(host(dk[:, :1]), r["dk"], "dk")
+    check_grad(host(dv[:, :1]), r["dv"], "dv")
+    n, B = w.n, w.block
+    nb = n // B
+    picks = [0, nb // 3, nb - 1]
+    blocks = [(0, b * B) for b in picks] + [(0, n + b * B) for b in picks + [nb // 2, 1]]
+    rows = np.concatenate([np.arange(r0, r0 + B) for _, r0 in blocks])
+    rs = oracle.bdlm_attention(host(x.q), host(x.k), host(x.v), B, w.scale, do=host(x.do), row_blocks=blocks,
+                               want_kv_grads=False)
+    check_o(host(o)[rows], rs["o"][rows], "sampled o")
+    check_lse(host(lse)[:, rows], rs["lse"][:, rows], "sampled lse")
+    check_grad(host(dq)[rows], rs["dq"][rows], "sampled dq")
