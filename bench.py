@@ -294,7 +294,9 @@ def run_cuda(args, rank, world, local):
     bd.load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = WORKLOAD
+    w = synth.BY_NAME[args.workload]
+    if not w.shards:
+        w = synth.Workload(**{**w.__dict__, "shards": 8})
     log(f"[rank {rank}] generating inputs for {w.name}")
     x = synth.make_inputs(w, device="cuda")
     step = Step(bd, w, x, dev)
@@ -330,7 +332,19 @@ def run_cuda(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = flops * world * args.steps / (total_ms / 1e3) / 1e12
 
-    # end to end through the public API: pinned host inputs in, results out
+    peaks, peak_kind = load_peaks()
+    achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(step, x, flops, args, world, dev)
+    _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks)
+
+
+def end_to_end(step, x, flops, args, world, dev):
+    """Same step through the public API with host buffers: pinned inputs are
+    copied in and every result copied out inside the timed region."""
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
     h_in = [pin(t) for t in (x.q, x.k, x.v, x.do)]
     for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
@@ -356,10 +370,19 @@ def run_cuda(args, rank, world, local):
     barrier(world, dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = flops * world * e2e_steps / (e2e_ms / 1e3) / 1e12
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps}
 
-    peaks, peak_kind = load_peaks()
-    achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+
+def l2_note(x):
+    qb = x.q.numel() * x.q.element_size()
+    if qb > 129e6:
+        return f"inputs larger than L2 (q alone {qb / 1e9:.2f} GB > 129 MB L2), no flush"
+    return f"inputs smaller than L2 (q {qb / 1e6:.0f} MB): profiling case, not a bench line"
+
+
+def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks):
     traffic = None
     if TRAFFIC["sha1"] and TRAFFIC["kernel_source"] and source_sha(TRAFFIC["kernel_source"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -370,7 +393,7 @@ def run_cuda(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "n_clean": w.n, "n_corrupted": w.n, "block": w.block, "heads": w.heads,
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "clean_shards": w.shards,
-                   "l2": "inputs larger than L2 (q alone 2.1 GB), no flush", "parallelism": f"replicas{world}"},
+                   "l2": l2_note(x), "parallelism": f"replicas{world}"},
         "roofline": {"kernel": "bdlm_attn_bwd (key-major main kernel + preprocess + dq convert)",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -384,8 +407,7 @@ def run_cuda(args, rank, world, local):
             "bwd_frac_bf16": f_bwd / (bwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
             "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
         },
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -410,6 +432,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--workload", default=WORKLOAD.name,
+                    help="workload name from synth (default: the 128K workload; others are for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         log("bench.py: at least 3 warm-up steps are required; using 3")

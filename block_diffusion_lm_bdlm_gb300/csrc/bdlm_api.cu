@@ -45,6 +45,7 @@ size_t sched_bytes(long long L, int n_docs) {
     b += round_up((size_t)mt * sizeof(Tile), 256);  // table
     b += round_up((size_t)mt * sizeof(Tile), 256);  // tmp
     b += round_up((size_t)mt * sizeof(int), 256);   // cost
+    b += 2 * round_up((size_t)mt * sizeof(TileRange), 256);  // ranges, rng_tmp
     return b;
 }
 
@@ -60,6 +61,10 @@ WsCarve carve(void* ws, long long L, int n_docs, int H, int d, bool bwd) {
     p += round_up((size_t)mt * sizeof(Tile), 256);
     c.cost = reinterpret_cast<int*>(p);
     p += round_up((size_t)mt * sizeof(int), 256);
+    c.ranges = reinterpret_cast<TileRange*>(p);
+    p += round_up((size_t)mt * sizeof(TileRange), 256);
+    c.rng_tmp = reinterpret_cast<TileRange*>(p);
+    p += round_up((size_t)mt * sizeof(TileRange), 256);
     c.max_tiles = (int)mt;
     if (bwd) {
         c.D = reinterpret_cast<float*>(p);
@@ -190,7 +195,7 @@ int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
     a.Lk = cm.Lk;
     a.table = ws.table;
     a.hdr = ws.hdr;
-    if (launch_fwd(a, sms, s, &launches) != cudaSuccess) return BDLM_ERR_CUDA;
+    if (launch_fwd_tc(a, ws.ranges, sms, s, &launches) != cudaSuccess) return BDLM_ERR_CUDA;
     g_launches = launches;
     return BDLM_OK;
 }

@@ -59,6 +59,15 @@ struct Span {
     int p_lo, p_hi, d_lo, d_hi;
 };
 
+// Key ranges of a whole tile, in k rows: every row's prefix interval lies in
+// [r1_lo, r1_hi) and every own-block interval in [r2_lo, r2_hi) (empty ranges
+// are [0, 0)); a key window [k0, k0 + w) inside [full_lo, full_hi) is visible
+// to every valid row of the tile, so it needs no element mask.
+struct TileRange {
+    int r1_lo, r1_hi, r2_lo, r2_hi;
+    int full_lo, full_hi, pad0, pad1;
+};
+
 __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 
@@ -98,9 +107,53 @@ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r
     return s;
 }
 
+// Exact key ranges of tile t: one span per diffusion block of rows (all rows
+// of a block share one span).
+__device__ __forceinline__ TileRange tile_range(const Layout& lay, const Tile& t) {
+    TileRange g{0x7fffffff, 0, 0x7fffffff, 0, 0, 0x7fffffff, 0, 0};
+    const int B = lay.B;
+    for (int r = 0; r < t.nrows;) {
+        const Span s = row_span(lay, t, r);
+        if (s.p_hi > s.p_lo) {
+            g.r1_lo = imin(g.r1_lo, s.p_lo);
+            g.r1_hi = imax(g.r1_hi, s.p_hi);
+            g.full_lo = imax(g.full_lo, s.p_lo);
+            g.full_hi = imin(g.full_hi, s.p_hi);
+        } else {
+            g.full_hi = 0;
+        }
+        if (s.d_hi > s.d_lo) {
+            g.r2_lo = imin(g.r2_lo, s.d_lo);
+            g.r2_hi = imax(g.r2_hi, s.d_hi);
+        }
+        const int pos = t.pos0 + r;
+        const int nxt = (pos / B + 1) * B - t.pos0;  // first row of the next block
+        r = nxt > r ? nxt : r + 1;
+    }
+    if (g.r1_hi == 0) g.r1_lo = 0;
+    if (g.r2_hi == 0) g.r2_lo = 0;
+    if (g.full_hi < g.full_lo) { g.full_lo = 0; g.full_hi = 0; }
+    return g;
+}
+
 __device__ __forceinline__ bool span_sees(const Span& s, int kr) {
     return (kr >= s.p_lo && kr < s.p_hi) || (kr >= s.d_lo && kr < s.d_hi);
 }
+
+// The one interval a key tile of a forward range is masked with: the prefix
+// interval while iterating the prefix range, the own-block interval while
+// iterating the own-block range. (The last tile of the prefix range may run
+// past the clean keys into own-block keys; those are counted by the own-block
+// range only.) Returned as [lo, lo + len) relative to the tile's first key k0.
+struct RelInterval {
+    int lo;
+    unsigned len;
+};
+__device__ __forceinline__ RelInterval range_interval(const Span& s, bool prefix, int k0) {
+    const int lo = prefix ? s.p_lo : s.d_lo, hi = prefix ? s.p_hi : s.d_hi;
+    return RelInterval{lo - k0, (unsigned)(hi > lo ? hi - lo : 0)};
+}
+__device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) { return (unsigned)(e - r.lo) < r.len; }
 
 __device__ __forceinline__ void set_error(WsHeader* h, int code, int info) {
     if (atomicCAS(&h->error, 0, code) == 0) atomicExch(&h->info, info);

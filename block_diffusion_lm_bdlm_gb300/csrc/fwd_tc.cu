@@ -1,0 +1,451 @@
+// fwd_tc.cu - BDLM attention forward on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+//
+// One persistent CTA per SM takes work items (128-row query tile, pair of
+// query heads that share one kv head) from the ordered tile list. Both heads
+// of a pair see the same keys under the same mask, so one K/V stream in
+// shared memory feeds two 128-row MMA tiles.
+//
+// Warp roles (384 threads, launched at 168 registers each):
+//   warps 0-3  softmax group 0 (head h0), one TMEM lane = one query row each
+//   warps 4-7  softmax group 1 (head h0 + 1)
+//   warp  8    TMA producer: Q tiles once per item, K/V tiles into a 2-stage ring
+//   warp  9    TMEM owner and MMA issuer (one thread)
+//   warps 10-11 spare (they only give their registers away)
+// Register budget: warps 8-11 drop to 56 registers and the eight softmax warps
+// rise to 224: 8 x 224 + 4 x 56 = 12 x 168, and per SM sub-partition
+// (warps w, w+4, w+8) 224 + 224 + 56 = 504 <= 512.
+// TMEM (512 columns): S0 | S1 | O0 | O1; P_i (bf16) overwrites the first 64
+// columns of S_i after the softmax group has read S_i into registers.
+// Per key tile j (128 keys):  S_i = Q_i K_j^T  ->  softmax_i  ->  O_i += P_i V_j.
+// The next S_i is issued only after the previous O_i += P_i V MMA has
+// completed (it reads P_i, which S_i overwrites); with two heads in flight the
+// tensor pipe stays fed during that wait.
+// Online softmax in fp32 registers, base 2, with a lazily moved offset: the
+// running row offset changes only when the row max exceeds it by more than
+// 2^8, and only then is the O row in TMEM rescaled.
+// Every mbarrier wait is bounded (2 s); a timeout sets the workspace error
+// word to BDLM_ERR_TIMEOUT and all roles drain out.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace bdlm {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (MMA M)
+constexpr int BN = 128;  // keys per step (MMA N of S = Q K^T)
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsOther = 56;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+template <int D>
+struct Lay {
+    static constexpr int kTile = BM * D * 2;       // bytes of a 128-row tile
+    static constexpr int kChunk = BM * 128;        // bytes of a 64-column, 128-row swizzled chunk
+    static constexpr int kQ0 = 0;
+    static constexpr int kQ1 = kTile;
+    static constexpr int kK = 2 * kTile;           // + stage * kTile
+    static constexpr int kV = 4 * kTile;           // + stage * kTile
+    static constexpr int kBytes = 6 * kTile + 1024;  // + alignment slack
+};
+
+// barrier slots
+enum : int { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_S = 7, B_P = 9, B_O = 11, B_COUNT = 13 };
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ int key_start(const TileRange& R, int n1, int j) {
+    return j < n1 ? R.r1_lo + j * BN : R.r2_lo + (j - n1) * BN;
+}
+
+struct ItemCtx {
+    Tile T;
+    TileRange R;
+    int n1, nk;
+    int kvh, h0;
+    bool two;
+    int q_row0;
+};
+
+// ---------------------------------------------------------------- producer
+template <int D>
+__device__ __forceinline__ void produce(const ItemCtx& c, uint32_t sbase, const uint64_t* bar,
+                                        const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                        uint32_t t_base, volatile int* abort) {
+    using S = Lay<D>;
+    constexpr int NC = D / 64;
+    const uint32_t bq = tc::smem_addr(&bar[B_Q]);
+    tc::mbar_arrive_expect_tx(bq, (c.two ? 2 : 1) * S::kTile);
+    for (int ch = 0; ch < NC; ++ch) {
+        tc::tma_load_3d(sbase + S::kQ0 + ch * S::kChunk, tq, bq, 64 * ch, c.h0, c.q_row0);
+        if (c.two) tc::tma_load_3d(sbase + S::kQ1 + ch * S::kChunk, tq, bq, 64 * ch, c.h0 + 1, c.q_row0);
+    }
+    for (int j = 0; j < c.nk; ++j) {
+        const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_KVEMPTY + s]), ph ^ 1, abort, kTimeoutNs)) return;
+        const int k0 = key_start(c.R, c.n1, j);
+        const uint32_t bk = tc::smem_addr(&bar[B_KFULL + s]), bv = tc::smem_addr(&bar[B_VFULL + s]);
+        tc::mbar_arrive_expect_tx(bk, S::kTile);
+        for (int ch = 0; ch < NC; ++ch)
+            tc::tma_load_3d(sbase + S::kK + s * S::kTile + ch * S::kChunk, tk, bk, 64 * ch, c.kvh, k0);
+        tc::mbar_arrive_expect_tx(bv, S::kTile);
+        for (int ch = 0; ch < NC; ++ch)
+            tc::tma_load_3d(sbase + S::kV + s * S::kTile + ch * S::kChunk, tv, bv, 64 * ch, c.kvh, k0);
+    }
+}
+
+// --------------------------------------------------------------------- MMA
+template <int D>
+__device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
+                                          uint32_t t_base, uint32_t t_base1, uint32_t q_count,
+                                          volatile int* abort) {
+    using S = Lay<D>;
+    constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, 0);
+    constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, 1);
+    if (!tc::mbar_wait(tc::smem_addr(&bar[B_Q]), q_count & 1, abort, kTimeoutNs)) return;
+    tc::tc_fence_after();
+    const int nh = c.two ? 2 : 1;
+    for (int j = 0; j < c.nk; ++j) {
+        const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + s]), ph, abort, kTimeoutNs)) return;
+        tc::tc_fence_after();
+        const uint32_t sK = sbase + S::kK + s * S::kTile;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (i >= nh) break;
+            const uint32_t ti = i == 0 ? t : t_base1 + j;
+            const uint32_t tS = tmem + 128 * i;
+            const uint32_t sQ = sbase + (i == 0 ? S::kQ0 : S::kQ1);
+            if (j > 0) {  // O_i += P_i V of the previous tile has read P_i
+                if (!tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), (ti - 1) & 1, abort, kTimeoutNs)) return;
+                tc::tc_fence_after();
+            }
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * S::kChunk + (k & 3) * 32;
+                tc::mma_ss(tS, tc::sdesc_sw128(sQ + off, 16, 1024), tc::sdesc_sw128(sK + off, 16, 1024), idesc_s,
+                           k > 0);
+            }
+            tc::mma_commit(tc::smem_addr(&bar[B_S + i]));
+        }
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_VFULL + s]), ph, abort, kTimeoutNs)) return;
+        const uint32_t sV = sbase + S::kV + s * S::kTile;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (i >= nh) break;
+            const uint32_t ti = i == 0 ? t : t_base1 + j;
+            const uint32_t tS = tmem + 128 * i, tO = tmem + 256 + D * i;
+            if (!tc::mbar_wait(tc::smem_addr(&bar[B_P + i]), ti & 1, abort, kTimeoutNs)) return;
+            tc::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o,
+                           (j > 0 || k > 0) ? 1u : 0u);
+            tc::mma_commit(tc::smem_addr(&bar[B_O + i]));
+        }
+        tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));
+    }
+}
+
+// ----------------------------------------------------------------- softmax
+// One thread per query row of head h0 + i. Reads S_i, writes P_i (bf16) back
+// into TMEM, keeps the row offset and sum, rescales O_i when the offset moves,
+// and finally normalises O_i and stores o and lse. TMEM loads and stores are
+// warp-collective, so every branch around them is warp-uniform.
+template <int D>
+__device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a, const uint64_t* bar, uint32_t tmem,
+                                             int i, uint32_t tb, volatile int* abort) {
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_base = (uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16;
+    const uint32_t tS = tmem + i * 128 + lane_base;
+    const uint32_t tO = tmem + 256 + i * D + lane_base;
+    const int h = c.h0 + i;
+    const Span sp = row_span(a.lay, c.T, row);
+    const float sl2 = a.scale_log2;
+    float m_use = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < c.nk; ++j) {
+        const uint32_t t = tb + j;
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_S + i]), t & 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc::tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_ld32(tS + 32 * q, r[q]);
+        tc::tmem_ld_wait();
+        float x[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[32 * q + e] = __uint_as_float(r[q][e]);
+        const int k0 = key_start(c.R, c.n1, j);
+        const bool full = j < c.n1 && k0 >= c.R.full_lo && k0 + BN <= c.R.full_hi;
+        if (!full) {
+            const RelInterval ri = range_interval(sp, j < c.n1, k0);
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+                if (!rel_sees(ri, e)) x[e] = -INFINITY;
+        }
+        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+        for (int e = 4; e < 128; e += 4) {
+            mx0 = fmaxf(mx0, x[e]);
+            mx1 = fmaxf(mx1, x[e + 1]);
+            mx2 = fmaxf(mx2, x[e + 2]);
+            mx3 = fmaxf(mx3, x[e + 3]);
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool move = mx > m_use + 8.0f;
+        float alpha = 1.f;
+        if (move) {
+            alpha = ex2f(m_use - mx);
+            l *= alpha;
+            m_use = mx;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tc::tmem_ld32(tO + 32 * q, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tc::tmem_st32(tO + 32 * q, o);
+            }
+        }
+        const float m_eff = m_use == -INFINITY ? 0.f : m_use;
+        float s0 = 0.f, s1 = 0.f;
+        uint32_t pa[32], pb[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2f(fmaf(x[2 * e], sl2, -m_eff));
+            const float p1 = ex2f(fmaf(x[2 * e + 1], sl2, -m_eff));
+            s0 += p0;
+            s1 += p1;
+            pa[e] = pack2(p0, p1);
+        }
+        tc::tmem_st32(tS, pa);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2f(fmaf(x[64 + 2 * e], sl2, -m_eff));
+            const float p1 = ex2f(fmaf(x[64 + 2 * e + 1], sl2, -m_eff));
+            s0 += p0;
+            s1 += p1;
+            pb[e] = pack2(p0, p1);
+        }
+        tc::tmem_st32(tS + 32, pb);
+        l += s0 + s1;
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_P + i]));
+    }
+    if (ok && c.nk > 0) {
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), (tb + c.nk - 1) & 1, abort, kTimeoutNs);
+        ok = __all_sync(0xffffffffu, got);
+        tc::tc_fence_after();
+    }
+    const bool have_o = ok && c.nk > 0;  // warp-uniform
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool store = row < c.T.nrows;
+    __nv_bfloat16* orow = a.o + ((long long)c.q_row0 + row) * ((long long)a.H * D) + (long long)h * D;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        if (have_o) {
+            tc::tmem_ld32(tO + 32 * q, o);
+            tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float* f = reinterpret_cast<const float*>(&o[8 * e]);
+                dst[e] = make_uint4(pack2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                                    pack2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                                    pack2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                                    pack2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                (void)f;
+            }
+        }
+    }
+    if (store)
+        a.lse[(long long)h * a.Lq + c.q_row0 + row] =
+            l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+}
+
+// ------------------------------------------------------------------ kernel
+__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+__device__ __forceinline__ ItemCtx decode(const FwdArgs& a, const TileRange* ranges, int item, int n_pairs,
+                                          int per_kv) {
+    ItemCtx c;
+    const int ti = item / n_pairs, pr = item % n_pairs;
+    c.T = a.table[ti];
+    c.R = ranges[ti];
+    c.kvh = pr / per_kv;
+    const int hp = pr % per_kv;
+    c.h0 = c.kvh * a.G + 2 * hp;
+    c.two = 2 * hp + 1 < a.G;
+    c.n1 = (c.R.r1_hi - c.R.r1_lo + BN - 1) / BN;
+    c.nk = c.n1 + (c.R.r2_hi - c.R.r2_lo + BN - 1) / BN;
+    c.q_row0 = c.T.doc_start + c.T.pos0;
+    return c;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a, const TileRange* __restrict__ ranges) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = tc::smem_addr(smem);
+    __shared__ __align__(8) uint64_t bar[B_COUNT];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_item;
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        s_abort = 0;
+        tc::mbar_init(tc::smem_addr(&bar[B_Q]), 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(tc::smem_addr(&bar[B_KFULL + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_VFULL + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_KVEMPTY + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_S + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_P + s]), 128);
+            tc::mbar_init(tc::smem_addr(&bar[B_O + s]), 1);
+        }
+        tc::fence_barrier_init();
+    }
+    if (warp == 9) {
+        tc::tmem_alloc(tc::smem_addr(&s_tmem), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort = &s_abort;
+
+    const int per_kv = (a.G + 1) / 2;
+    const int n_pairs = a.Hk * per_kv;
+    const int n_items = a.hdr->n_tiles * n_pairs;
+    uint32_t t_base = 0, t_base1 = 0, q_count = 0;
+    // Two register regions: each role branch runs its own copy of the item
+    // loop; the branches meet at named barrier 1 (all 384 threads) twice per item.
+    if (warp >= 8) {
+        tc::regs_dec<kRegsOther>();
+        for (;;) {
+            named_sync();
+            if (tid == 256) s_item = *abort ? n_items : atomicAdd(&a.hdr->counter, 1);
+            named_sync();
+            const int item = s_item;
+            if (item >= n_items) break;
+            const ItemCtx c = decode(a, ranges, item, n_pairs, per_kv);
+            if (warp == 8 && lane == 0 && c.nk > 0) produce<D>(c, sbase, bar, &tm_q, &tm_k, &tm_v, t_base, abort);
+            if (warp == 9 && lane == 0 && c.nk > 0)
+                issue_mma<D>(c, sbase, bar, tmem, t_base, t_base1, q_count, abort);
+            t_base += c.nk;
+            if (c.two) t_base1 += c.nk;
+            if (c.nk > 0) ++q_count;
+        }
+    } else {
+        tc::regs_inc<kRegsSoftmax>();
+        const int wg = warp >> 2;
+        for (;;) {
+            named_sync();
+            named_sync();
+            const int item = s_item;
+            if (item >= n_items) break;
+            const ItemCtx c = decode(a, ranges, item, n_pairs, per_kv);
+            if (wg == 0 || c.two) softmax_rows<D>(c, a, bar, tmem, wg, wg == 0 ? t_base : t_base1, abort);
+            t_base += c.nk;
+            if (c.two) t_base1 += c.nk;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && s_abort) set_error(a.hdr, DEV_TIMEOUT, blockIdx.x);
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [rows, heads, D] bf16 tensor as a 3-D map (D, heads, rows) with 64 x 1 x 128 boxes, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int heads, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)BM};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, D, a.H, a.Lq) || !make_map(&mk, a.k, D, a.Hk, a.Lk) || !make_map(&mv, a.v, D, a.Hk, a.Lk))
+        return cudaErrorInvalidValue;
+    constexpr int smem = Lay<D>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fwd_tc_kernel<D><<<num_sms, kThreads, smem, st>>>(mq, mk, mv, a, ranges);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st, int* launches) {
+    cudaError_t e = a.D == 128 ? launch_tc<128>(a, ranges, num_sms, st) : launch_tc<64>(a, ranges, num_sms, st);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+}
+
+}  // namespace bdlm

@@ -11,6 +11,8 @@ struct WsCarve {
     Tile* table;    // ordered tiles
     Tile* tmp;      // unordered tiles (prologue scratch)
     int* cost;      // per-tile cost (prologue scratch)
+    TileRange* ranges;   // key ranges of the ordered tiles (forward)
+    TileRange* rng_tmp;  // key ranges of the unordered tiles (prologue scratch)
     int max_tiles;
     float* D;       // backward: rowsum(dO * o), [H, L]
     float* dqacc;   // backward: fp32 dq accumulator, [L, H, d]
@@ -62,14 +64,14 @@ struct MergeArgs {
 };
 
 // Tile heights used by the kernels (the prologue enumerates in these units).
-constexpr int kFwdTileRows = 64;
-constexpr int kFwdKeyTile = 64;
+constexpr int kFwdTileRows = 128;  // tensor-core forward: 128-row query tiles
+constexpr int kFwdKeyTile = 128;   // and 128-key steps
 constexpr int kBwdKeyTile = 64;
 constexpr int kBwdQTile = 64;
 
 void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, const WsCarve& ws,
                       cudaStream_t st);
-cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t st, int* launches);
+cudaError_t launch_fwd_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st, int* launches);
 

@@ -62,21 +62,8 @@ __device__ void doc_of(const Layout& lay, int d, int* start, int* n) {
 }
 
 // Cost of a forward query tile, in key tiles of kn rows.
-__device__ int fwd_cost(const Layout& lay, const Tile& t, int kn) {
-    int len = 0;
-    if (lay.mode == MODE_GROUP) {
-        int b0 = t.pos0 / lay.B, b1 = (t.pos0 + t.nrows - 1) / lay.B;
-        int bmax = 0;
-        for (int i = b0; i <= b1; ++i) bmax = imax(bmax, __ldg(lay.blocks + i));
-        len = (bmax * lay.B + kn - 1) / kn + (t.nrows + lay.B + kn - 1) / kn;
-        return len;
-    }
-    Span a = row_span(lay, t, 0), z = row_span(lay, t, t.nrows - 1);
-    int p_lo = a.p_hi > a.p_lo ? a.p_lo : z.p_lo;
-    int p = z.p_hi > z.p_lo ? (z.p_hi - p_lo + kn - 1) / kn : 0;
-    int d_lo = a.d_hi > a.d_lo ? a.d_lo : z.d_lo;
-    int dd = z.d_hi > z.d_lo ? (z.d_hi - d_lo + kn - 1) / kn : 0;
-    return p + dd;
+__device__ int fwd_cost(const TileRange& g, int kn) {
+    return (g.r1_hi - g.r1_lo + kn - 1) / kn + (g.r2_hi - g.r2_lo + kn - 1) / kn;
 }
 
 // Cost of a backward key tile, in query rows that see it.
@@ -92,7 +79,8 @@ __device__ int bwd_cost(const Layout& lay, const Tile& t) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table, Tile* tmp,
-                 int* cost_tmp, WsHeader* hdr, int max_tiles, int cost_shift) {
+                 int* cost_tmp, TileRange* ranges, TileRange* rng_tmp, WsHeader* hdr, int max_tiles,
+                 int cost_shift) {
     __shared__ int hist[kBuckets];
     __shared__ int sbuf[96];
     __shared__ int s_carry;
@@ -137,14 +125,8 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     if (lay.mode == MODE_GROUP) {
         const int rows = lay.n_blocks * lay.B;
         const int nt = (rows + tile_rows - 1) / tile_rows;
-        for (int i = tid; i < nt; i += kThreads) {
-            Tile t{0, lay.n, i * tile_rows, imin(tile_rows, rows - i * tile_rows)};
-            int c = fwd_cost(lay, t, key_tile) >> cost_shift;
-            c = imin(c, kBuckets - 1);
-            tmp[i] = t;
-            cost_tmp[i] = c;
-            atomicAdd(&hist[c], 1);
-        }
+        for (int i = tid; i < nt && i < max_tiles; i += kThreads)
+            tmp[i] = Tile{0, lay.n, i * tile_rows, imin(tile_rows, rows - i * tile_rows)};
         if (tid == 0) s_carry = nt;
         __syncthreads();
     } else {
@@ -162,15 +144,8 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
                 for (int i = 0; i < 2 * per_half; ++i) {
                     const int half = i / per_half, j = i % per_half;
                     const int p0 = half * n + j * tile_rows;
-                    Tile t{start, n, p0, imin(tile_rows, (half + 1) * n - p0)};
-                    int c = kind == 0 ? fwd_cost(lay, t, key_tile) : bwd_cost(lay, t);
-                    c = imin(c >> cost_shift, kBuckets - 1);
                     const int idx = carry + off + i;
-                    if (idx < max_tiles) {
-                        tmp[idx] = t;
-                        cost_tmp[idx] = c;
-                        atomicAdd(&hist[c], 1);
-                    }
+                    if (idx < max_tiles) tmp[idx] = Tile{start, n, p0, imin(tile_rows, (half + 1) * n - p0)};
                 }
             }
             __syncthreads();
@@ -182,6 +157,23 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     if (n_tiles > max_tiles) {
         if (tid == 0) set_error(hdr, DEV_CHECK, -2);
         return;
+    }
+    __syncthreads();
+
+    // ---- exact ranges and costs -------------------------------------------------
+    for (int i = tid; i < n_tiles; i += kThreads) {
+        const Tile t = tmp[i];
+        int c;
+        if (kind == 0) {
+            const TileRange g = tile_range(lay, t);
+            rng_tmp[i] = g;
+            c = fwd_cost(g, key_tile);
+        } else {
+            c = bwd_cost(lay, t);
+        }
+        c = imin(c >> cost_shift, kBuckets - 1);
+        cost_tmp[i] = c;
+        atomicAdd(&hist[c], 1);
     }
     __syncthreads();
 
@@ -206,6 +198,7 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     for (int i = tid; i < n_tiles; i += kThreads) {
         int pos = atomicAdd(&hist[cost_tmp[i]], 1);
         table[pos] = tmp[i];
+        if (kind == 0) ranges[pos] = rng_tmp[i];
     }
     if (tid == 0) hdr->n_tiles = n_tiles;
 }
@@ -219,8 +212,8 @@ void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, 
     long long max_cost = kind == 0 ? (2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n)) / key_tile + 4
                                    : 2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n);
     while ((max_cost >> shift) >= kBuckets) ++shift;
-    enumerate_kernel<<<1, kThreads, 0, st>>>(lay, tile_rows, key_tile, kind, ws.table, ws.tmp,
-                                             ws.cost, ws.hdr, ws.max_tiles, shift);
+    enumerate_kernel<<<1, kThreads, 0, st>>>(lay, tile_rows, key_tile, kind, ws.table, ws.tmp, ws.cost,
+                                             ws.ranges, ws.rng_tmp, ws.hdr, ws.max_tiles, shift);
 }
 
 }  // namespace bdlm

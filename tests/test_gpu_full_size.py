@@ -1,0 +1,162 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times. The oracle checks sampled query blocks one by one (o, lse
+and dq are row-local), complete dk/dv for sampled key blocks (every query
+block that sees them is recomputed), and identities that hold at any size:
+sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per kv head."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import check_grad, check_lse, check_o, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bd():
+    import block_diffusion_lm_bdlm_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def group_slices(x, w, g):
+    G = w.heads // w.kv_heads
+    return x.q[:, g * G:(g + 1) * G], x.k[:, g:g + 1], x.v[:, g:g + 1], x.do[:, g * G:(g + 1) * G]
+
+
+def f32(t):
+    return t.float().cpu().numpy()
+
+
+def sampled_rows_check(x, w, o, lse, dq, kv_groups, blocks, cu=None):
+    """o, lse, dq of the given query blocks (doc, first row) against the oracle."""
+    G = w.heads // w.kv_heads
+    for g in kv_groups:
+        q, k, v, do = (f32(t) for t in group_slices(x, w, g))
+        r = oracle.bdlm_attention(q, k, v, w.block, w.scale, cu_seqlens=cu, do=do, row_blocks=blocks,
+                                  want_kv_grads=False)
+        starts = [0] if cu is None else cu
+        rows = np.concatenate([starts[d] + np.arange(r0, r0 + w.block) for d, r0 in blocks])
+        hs = slice(g * G, (g + 1) * G)
+        check_o(host(o[rows][:, hs]), r["o"][rows], f"o (kv group {g})")
+        check_lse(host(lse[hs][:, rows]), r["lse"][:, rows], f"lse (kv group {g})")
+        check_grad(host(dq[rows][:, hs]), r["dq"][rows], f"dq (kv group {g})")
+
+
+def sampled_keys_check(x, w, dk, dv, g, n, key_blocks):
+    """Complete dk, dv of the clean key block b_c (seen by clean blocks >= b_c
+    and corrupted blocks > b_c) and of corrupted key blocks (seen by their own
+    block), for kv group g."""
+    B = w.block
+    nb = n // B
+    q, k, v, do = (f32(t) for t in group_slices(x, w, g))
+    for kind, b in key_blocks:
+        if kind == "clean":
+            seers = [(0, bb * B) for bb in range(b, nb)] + [(0, n + bb * B) for bb in range(b + 1, nb)]
+            keys = np.arange(b * B, (b + 1) * B)
+        else:
+            seers = [(0, n + b * B)]
+            keys = n + np.arange(b * B, (b + 1) * B)
+        r = oracle.bdlm_attention(q, k, v, B, w.scale, do=do, row_blocks=seers)
+        check_grad(host(dk[keys][:, g:g + 1]), r["dk"][keys], f"dk {kind} block {b}")
+        check_grad(host(dv[keys][:, g:g + 1]), r["dv"][keys], f"dv {kind} block {b}")
+
+
+def identities_check(x, w, dk, dv):
+    G = w.heads // w.kv_heads
+    dk64 = dk.double()
+    s = dk64.sum(0)                                   # [Hk, d]
+    scale = dk64.abs().sum(0)
+    assert (s.abs() <= 1e-2 * scale + 1e-3).all(), "sum of dK over keys is not ~0"
+    dv_sum = dv.double().sum(0)
+    do_sum = x.do.double().view(x.do.shape[0], w.kv_heads, G, -1).sum((0, 2))
+    rel = (dv_sum - do_sum).norm() / do_sum.norm()
+    assert rel <= 1e-2, f"sum of dV differs from sum of dO: {rel:.3e}"
+
+
+def test_long128k_sharded_forward_merge_backward(bd):
+    w = synth.BY_NAME["long128k_n131072_b64_h32kv8_d128"]
+    x = synth.make_inputs(w, device="cuda")
+    n, B = w.n, w.block
+    windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+    parts, lses = [], []
+    for lo, hi in windows:
+        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], B, part=bd.Partial.window(lo, hi))
+        parts.append(po)
+        lses.append(pl)
+    o, lse = bd.bdlm_lse_merge(parts, lses)
+    del parts
+    uo, ul = bd.bdlm_attn_fwd(x.q, x.k, x.v, B)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B)
+    torch.cuda.synchronize()
+    # sharded + merged == unsharded (both on the GPU)
+    assert (o.float() - uo.float()).abs().max().item() <= 2e-2
+    assert ((lse - ul).abs() / ul.abs().clamp(min=1.0)).max().item() <= 1e-3
+    del uo, ul
+    nb = n // B
+    blocks = [(0, 0), (0, (nb // 2) * B), (0, (nb - 1) * B), (0, n), (0, n + (nb // 3) * B), (0, n + (nb - 1) * B)]
+    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 7], blocks=blocks)
+    sampled_keys_check(x, w, dk, dv, g=3, n=n, key_blocks=[("clean", nb - 1), ("clean", nb - 2), ("corrupted", 0),
+                                                           ("corrupted", nb // 2)])
+    identities_check(x, w, dk, dv)
+
+
+def test_vlong256k_block_groups_and_backward(bd):
+    w = synth.BY_NAME["vlong256k_n262144_b16_h16kv4_d128"]
+    x = synth.make_inputs(w, device="cuda")
+    n, B = w.n, w.block
+    nb = n // B
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B)
+    groups = synth.early_late_groups(nb, w.groups)
+    worst_o, worst_l = 0.0, 0.0
+    clean_pos = torch.arange(n, device="cuda")
+    for blocks in groups:
+        bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
+        corr = (n + bl.long()[:, None] * B + torch.arange(B, device="cuda")[None]).reshape(-1)
+        kpos = torch.cat([clean_pos, corr])
+        go, gl = bd.bdlm_attn_fwd(x.q[corr].contiguous(), x.k[kpos].contiguous(), x.v[kpos].contiguous(), B,
+                                  L=2 * n, part=bd.Partial.group(bl))
+        torch.cuda.synchronize()
+        worst_o = max(worst_o, (go.float() - o[corr].float()).abs().max().item())
+        worst_l = max(worst_l, ((gl - lse[:, corr]).abs() / lse[:, corr].abs().clamp(min=1.0)).max().item())
+    assert worst_o <= 2e-2 and worst_l <= 1e-3, (worst_o, worst_l)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B)
+    torch.cuda.synchronize()
+    # the early/late pair of group 0 and a middle block, clean and corrupted
+    blocks = [(0, 0), (0, (nb - 1) * B), (0, n), (0, n + (nb - 1) * B), (0, n + (nb // 2) * B)]
+    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 3], blocks=blocks)
+    sampled_keys_check(x, w, dk, dv, g=1, n=n, key_blocks=[("clean", nb - 1), ("corrupted", 5)])
+    identities_check(x, w, dk, dv)
+
+
+def test_packed_documents_full_size(bd):
+    w = synth.BY_NAME["packed64_b32_h32kv8_d128"]
+    x = synth.make_inputs(w, device="cuda")
+    cu = x.cu_seqlens
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    B = w.block
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, cu_seqlens=cu_d)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, cu_seqlens=cu_d)
+    torch.cuda.synchronize()
+    lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    # two short documents in full (all gradients, one kv group)
+    short = sorted(range(len(lens)), key=lambda i: lens[i])[:2]
+    G = w.heads // w.kv_heads
+    for d in short:
+        s = slice(cu[d], cu[d + 1])
+        q, k, v, do = (f32(t[s]) for t in group_slices(x, w, 2))
+        r = oracle.bdlm_attention(q, k, v, B, w.scale, do=do)
+        check_o(host(o[s][:, 2 * G:3 * G]), r["o"])
+        check_lse(host(lse[2 * G:3 * G, s]), r["lse"])
+        check_grad(host(dq[s][:, 2 * G:3 * G]), r["dq"], "dq")
+        check_grad(host(dk[s][:, 2:3]), r["dk"], "dk")
+        check_grad(host(dv[s][:, 2:3]), r["dv"], "dv")
+    # sampled blocks of the longest document
+    big = max(range(len(lens)), key=lambda i: lens[i])
+    nd = lens[big] // 2
+    blocks = [(big, 0), (big, nd - B), (big, nd), (big, 2 * nd - B)]
+    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 5], blocks=blocks, cu=cu)
+    identities_check(x, w, dk, dv)

@@ -46,6 +46,8 @@ SHAPES = [
     (320, 32, 8, 2, 128),    # several tiles per half
     (200, 8, 3, 3, 64),      # odd head count, ragged
     (64, 64, 1, 1, 128),     # one tile of one block
+    (40, 8, 2, 1, 64),       # the prefix range's last key tile runs into own-block keys
+    (96, 16, 2, 2, 128),     # same, for 128-key tiles
 ]
 
 
