@@ -84,6 +84,7 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     __shared__ int hist[kBuckets];
     __shared__ int sbuf[96];
     __shared__ int s_carry;
+    __shared__ int s_off[kThreads];
     const int tid = threadIdx.x;
     if (tid == 0) {
         hdr->error = 0;
@@ -130,23 +131,36 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         if (tid == 0) s_carry = nt;
         __syncthreads();
     } else {
+        // documents in chunks of kThreads: scan the per-document tile counts,
+        // then let every thread fill tiles, finding its document by binary
+        // search over the chunk's tile offsets
         for (int base = 0; base < ndocs; base += kThreads) {
             const int d = base + tid;
+            const int nd = imin(kThreads, ndocs - base);
             int start = 0, n = 0, per_half = 0;
             if (d < ndocs) {
                 doc_of(lay, d, &start, &n);
                 per_half = (n + tile_rows - 1) / tile_rows;
             }
             int total;
-            int off = block_exclusive_scan(2 * per_half, &total, sbuf);
+            const int off = block_exclusive_scan(2 * per_half, &total, sbuf);
+            s_off[tid] = off;
+            __syncthreads();
             const int carry = s_carry;
-            if (d < ndocs) {
-                for (int i = 0; i < 2 * per_half; ++i) {
-                    const int half = i / per_half, j = i % per_half;
-                    const int p0 = half * n + j * tile_rows;
-                    const int idx = carry + off + i;
-                    if (idx < max_tiles) tmp[idx] = Tile{start, n, p0, imin(tile_rows, (half + 1) * n - p0)};
+            for (int i = tid; i < total; i += kThreads) {
+                int lo = 0, hi = nd - 1;  // last document whose offset <= i
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
                 }
+                int ds, dn;
+                doc_of(lay, base + lo, &ds, &dn);
+                const int ph = (dn + tile_rows - 1) / tile_rows;
+                const int li = i - s_off[lo];
+                const int half = li / ph, j = li % ph;
+                const int p0 = half * dn + j * tile_rows;
+                const int idx = carry + i;
+                if (idx < max_tiles) tmp[idx] = Tile{ds, dn, p0, imin(tile_rows, (half + 1) * dn - p0)};
             }
             __syncthreads();
             if (tid == 0) s_carry = carry + total;
