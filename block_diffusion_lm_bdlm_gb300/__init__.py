@@ -22,7 +22,7 @@ import torch
 from .build import LIB
 
 __all__ = [
-    "BDLMError", "Partial", "bdlm_attn_fwd", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
+    "BDLMError", "Partial", "bdlm_attn_fwd", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_last_launch_count",
     "load_library", "EXPORTED_SYMBOLS",
 ]
@@ -34,6 +34,7 @@ PART_NONE, PART_KEY_WINDOW, PART_BLOCK_GROUP = 0, 1, 2
 EXPORTED_SYMBOLS = (
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_attn_fwd", "bdlm_attn_bwd",
     "bdlm_lse_merge", "bdlm_read_error", "bdlm_status_string", "bdlm_last_launch_count",
+    "bdlm_attn_fwd_noalloc",
 )
 
 
@@ -97,6 +98,9 @@ def load_library() -> ctypes.CDLL:
     lib.bdlm_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, i32, f32,
                                   ctypes.POINTER(_CPartial), vp, sz, vp]
     lib.bdlm_attn_fwd.restype = ctypes.c_int
+    lib.bdlm_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, i32, f32,
+                                          ctypes.POINTER(_CPartial), vp]
+    lib.bdlm_attn_fwd_noalloc.restype = ctypes.c_int
     lib.bdlm_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp, i32, f32,
                                   ctypes.POINTER(_CPartial), vp, sz, vp]
     lib.bdlm_attn_bwd.restype = ctypes.c_int
@@ -176,6 +180,31 @@ def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=No
                            Hk, d, cu_ptr, n_docs, softmax_scale, cpart, workspace.data_ptr(),
                            workspace.numel(), _stream(stream))
     _check(st, "bdlm_attn_fwd")
+    return out, lse
+
+
+def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=None,
+                          softmax_scale: float = 0.0, part: Optional[Partial] = None, out=None, lse=None,
+                          stream=None):
+    """The forward without a workspace (see bdlm_attn_fwd_noalloc in
+    include/bdlm.h): the library uses its own fixed scratch, so the call
+    allocates nothing on the device beyond the outputs (pass `out` and `lse`
+    to allocate nothing at all)."""
+    lib = load_library()
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(nm, t)
+    Lq, H, d = q.shape
+    Hk = k.shape[1]
+    L = Lq if L is None else int(L)
+    cu_ptr, n_docs = _cu(cu_seqlens)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, Lq), dtype=torch.float32, device=q.device)
+    cpart = ctypes.byref(part.c()) if part is not None else None
+    st = lib.bdlm_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L,
+                                   block, H, Hk, d, cu_ptr, n_docs, softmax_scale, cpart, _stream(stream))
+    _check(st, "bdlm_attn_fwd_noalloc")
     return out, lse
 
 

@@ -121,6 +121,33 @@ BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o,
                   bdlm_stream_t stream);
 
 /*
+ * bdlm_attn_fwd_noalloc - the forward for callers that cannot allocate device
+ * memory where they call it: code under CUDA stream capture (cudaMalloc is not
+ * allowed there), plugins whose host framework owns every device allocation,
+ * services that forbid allocation after start-up. (The paper has no
+ * counterpart; this is a library convenience.)
+ *
+ * Same arguments and results as bdlm_attn_fwd, minus the workspace: the
+ * forward's scratch (tile table, work counter, device error word) lives in a
+ * fixed 4 MiB array inside the library, which every GPU that loads the
+ * library holds until the process exits. That bounds the call size: when
+ * bdlm_attn_fwd_workspace_bytes(L, heads, head_dim, n_docs) exceeds 4 MiB
+ * (about 2.6 million rows for one sequence) the call returns
+ * BDLM_ERR_WORKSPACE and launches nothing; use bdlm_attn_fwd then.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call on a device shares the one array and each call clears
+ * the parts that must start at zero; calls whose execution overlaps on the
+ * GPU (other streams, or other host threads) race on it, so order them.
+ * Device-detected errors land in the shared array and are not readable
+ * through bdlm_read_error.
+ */
+BDLM_API int bdlm_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                  const int32_t* cu_seqlens, int32_t n_docs, float softmax_scale,
+                  const bdlm_partial* part, bdlm_stream_t stream);
+
+/*
  * Backward of the full forward (part must be NULL or kind NONE): given q, k, v,
  * the forward's o and lse, and the upstream gradient dO, writes
  * dq [L, H, d], dk [L, Hk, d], dv [L, Hk, d] (bf16). dk and dv sum the
