@@ -222,7 +222,7 @@ int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
 
     WsCarve ws = carve(workspace, L, docs, heads, head_dim, true);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    launch_enumerate(lay, kBwdKeyTile, kBwdQTile, 1, ws, s);
+    launch_enumerate(lay, head_dim == 128 ? kBwdTcKeyTile : kBwdKeyTile, kBwdQTile, 1, ws, s);
     if (cudaGetLastError() != cudaSuccess) return BDLM_ERR_CUDA;
     int launches = 1;
 

@@ -1,4 +1,6 @@
-// bwd_mma.cu - BDLM attention backward on warp-level tensor cores.
+// bwd_mma.cu - BDLM attention backward: preprocess and dq-convert kernels,
+// and the warp-level tensor-core (mma.sync) main kernel used for head_dim 64
+// (head_dim 128 runs the tcgen05 main kernel of bwd_tc.cu).
 //
 // Three kernels after the tile prologue:
 //   1. preprocess: D_i = sum_d dO_i * o_i (fp32) per (row, head), and zero the
@@ -311,11 +313,15 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    constexpr int smem = bwd_smem_bytes<D>();
-    e = cudaFuncSetAttribute(bwd_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    bwd_mma_kernel<D><<<num_sms * 2, NT, smem, st>>>(a);
-    e = cudaGetLastError();
+    if (D == 128) {
+        e = launch_bwd_tc_main(a, num_sms, st);  // tensor-core main kernel, 128-key tiles
+    } else {
+        constexpr int smem = bwd_smem_bytes<D>();
+        e = cudaFuncSetAttribute(bwd_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        bwd_mma_kernel<D><<<num_sms * 2, NT, smem, st>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const long long cv = pairs * D / 8;
     bwd_convert_kernel<D><<<(unsigned)((cv + 255) / 256), 256, 0, st>>>(a);

@@ -1,0 +1,490 @@
+// bwd_tc.cu - BDLM attention backward main kernel on the 5th-generation
+// tensor cores (head_dim 128).
+//
+// Key-major: one work item = (128-key tile, kv head). The item loops over the
+// G query heads of the kv head and, for each, over the 64-row query steps
+// that see the key tile (a clean key tile is seen by the clean rows from its
+// block on and by the corrupted rows of later blocks; a corrupted key tile
+// only by its own blocks' corrupted rows). Per step:
+//   S^T  = K Q^T          (M 128 keys, N 64 rows, K = d)      -> TMEM
+//   dP^T = V dO^T                                              -> TMEM
+//   P^T  = exp2(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D)
+//          (compute warps; P^T and dS^T go back to TMEM as bf16, dS^T also
+//          to shared memory)
+//   dV  += P^T dO         (A from TMEM)                        -> TMEM
+//   dK  += dS^T Q         (A from TMEM)                        -> TMEM
+//   dQ^T = K^T dS^T       (M = d, N 64 rows, K 128 keys)       -> TMEM
+//          read out, scaled, staged in shared memory and added into the fp32
+//          dq accumulator with one TMA reduce-add per step.
+// dK and dV stay in TMEM for the whole item (no atomics: the item owns its
+// keys for all G heads) and are written once, as bf16, at the end.
+//
+// Warp roles (320 threads): warps 0-7 compute (two groups of 4 warps, one
+// TMEM lane = one key row; group g takes query columns 32g..32g+31 of a
+// step), warp 8 loads (TMA for K, V, Q, dO; plain loads for lse, D and the
+// query rows' key intervals), warp 9 owns TMEM and issues the MMAs.
+// TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
+// dQ^T [384,448). Every mbarrier wait is bounded (2 s).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace bdlm {
+namespace {
+
+constexpr int D = 128;
+constexpr int BN = 128;  // keys per item
+constexpr int BQ = 64;   // query rows per step
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TDQ = 384;
+
+// dynamic shared memory (1024-aligned offsets)
+constexpr int kKV = BN * D * 2;     // 32 KB: K or V tile, two 64-column chunks of 16 KB
+constexpr int kQT = BQ * D * 2;     // 16 KB: Q or dO tile, two chunks of 8 KB
+constexpr int SM_K = 0;
+constexpr int SM_V = SM_K + kKV;
+constexpr int SM_Q = SM_V + kKV;          // + stage * kQT
+constexpr int SM_O = SM_Q + 2 * kQT;      // + stage * kQT
+constexpr int SM_S = SM_O + 2 * kQT;      // dS^T [128 keys][64 rows] bf16, 128-byte swizzled rows
+constexpr int SM_STG = SM_S + BN * BQ * 2;  // dq staging [64 rows][128] fp32
+constexpr int kSmemBytes = SM_STG + BQ * D * 4 + 1024;
+
+enum : int {
+    B_KV = 0, B_QDF = 1, B_QDE = 3, B_S = 5, B_DP = 6, B_SM = 7, B_DV = 8, B_DK = 9, B_DQ = 10, B_DQF = 11,
+    B_COUNT = 12
+};
+
+struct StepInfo {
+    float lse2[BQ];  // lse * log2(e); +inf for rows without keys or beyond the step
+    float dsum[BQ];  // D = rowsum(dO * o)
+    Span span[BQ];
+    int full;        // every row sees every key of the tile
+    int pad[3];
+};
+
+struct ItemCtx {
+    Tile kt;
+    int kvh, k0, kv_rows;
+    int ra_lo, ra_hi, rb_lo, rb_hi, na, per_head, n_steps;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Barrier over the n threads of named barrier `id` that also ANDs a predicate,
+// so that a decision to stop is taken by all of them together.
+__device__ __forceinline__ bool named_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ ItemCtx decode(const BwdArgs& a, int item) {
+    ItemCtx c;
+    c.kt = a.table[item / a.Hk];
+    c.kvh = item % a.Hk;
+    const int n = c.kt.n, B = a.lay.B;
+    c.k0 = c.kt.doc_start + c.kt.pos0;
+    c.kv_rows = c.kt.nrows;
+    c.rb_lo = c.rb_hi = 0;
+    if (c.kt.pos0 < n) {
+        const int b = c.kt.pos0 / B;
+        c.ra_lo = b * B;
+        c.ra_hi = n;
+        c.rb_lo = n + (b + 1) * B;
+        c.rb_hi = 2 * n;
+    } else {
+        const int b0 = (c.kt.pos0 - n) / B, b1 = (c.kt.pos0 + c.kv_rows - 1 - n) / B;
+        c.ra_lo = n + b0 * B;
+        c.ra_hi = n + (b1 + 1) * B;
+    }
+    c.na = (c.ra_hi - c.ra_lo + BQ - 1) / BQ;
+    const int nb = c.rb_hi > c.rb_lo ? (c.rb_hi - c.rb_lo + BQ - 1) / BQ : 0;
+    c.per_head = c.na + nb;
+    c.n_steps = c.per_head * a.G;
+    return c;
+}
+
+// query rows of step s: head, first document position, valid rows
+__device__ __forceinline__ void step_rows(const ItemCtx& c, const BwdArgs& a, int s, int* h, int* p0, int* nrows) {
+    const int hh = s / c.per_head, rem = s % c.per_head;
+    *h = c.kvh * a.G + hh;
+    *p0 = rem < c.na ? c.ra_lo + rem * BQ : c.rb_lo + (rem - c.na) * BQ;
+    const int hi = rem < c.na ? c.ra_hi : c.rb_hi;
+    *nrows = imin(BQ, hi - *p0);
+}
+
+// ---------------------------------------------------------------- loader
+__device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, const uint64_t* bar,
+                                          StepInfo* info, const CUtensorMap* tk, const CUtensorMap* tv,
+                                          const CUtensorMap* tq, const CUtensorMap* tdo, uint32_t ts_base,
+                                          volatile int* abort) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        const uint32_t bkv = tc::smem_addr(&bar[B_KV]);
+        tc::mbar_arrive_expect_tx(bkv, 2 * kKV);
+        for (int ch = 0; ch < 2; ++ch) {
+            tc::tma_load_3d(sbase + SM_K + ch * (kKV / 2), tk, bkv, 64 * ch, c.kvh, c.k0);
+            tc::tma_load_3d(sbase + SM_V + ch * (kKV / 2), tv, bkv, 64 * ch, c.kvh, c.k0);
+        }
+    }
+    for (int s = 0; s < c.n_steps; ++s) {
+        const uint32_t ts = ts_base + s, st = ts & 1;
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + st]), ((ts >> 1) & 1) ^ 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) return;
+        int h, p0, nrows;
+        step_rows(c, a, s, &h, &p0, &nrows);
+        const int qr0 = c.kt.doc_start + p0;
+        const uint32_t bf = tc::smem_addr(&bar[B_QDF + st]);
+        if (lane == 0) {
+            mbar_expect_tx(bf, 2 * kQT);
+            for (int ch = 0; ch < 2; ++ch) {
+                tc::tma_load_3d(sbase + SM_Q + st * kQT + ch * (kQT / 2), tq, bf, 64 * ch, h, qr0);
+                tc::tma_load_3d(sbase + SM_O + st * kQT + ch * (kQT / 2), tdo, bf, 64 * ch, h, qr0);
+            }
+        }
+        StepInfo& inf = info[st];
+        const Tile qt{c.kt.doc_start, c.kt.n, p0, nrows};
+        bool rowfull = true;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int r = 2 * lane + u;
+            const Span sp = row_span(a.lay, qt, r);
+            float l2 = INFINITY, dd = 0.f;
+            if (r < nrows) {
+                const float lse = __ldg(a.lse + (long long)h * a.L + qr0 + r);
+                l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+                dd = __ldg(a.Dsum + (long long)h * a.L + qr0 + r);
+            }
+            inf.lse2[r] = l2;
+            inf.dsum[r] = dd;
+            inf.span[r] = sp;
+            rowfull = rowfull && r < nrows && sp.p_lo <= c.k0 && c.k0 + BN <= sp.p_hi;
+        }
+        const bool full = __all_sync(0xffffffffu, rowfull) && c.kv_rows == BN;
+        if (lane == 0) inf.full = full ? 1 : 0;
+        tc::mbar_arrive(bf);
+    }
+}
+
+// ------------------------------------------------------------------- MMA
+__device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
+                                           uint32_t ts_base, uint32_t item_count, volatile int* abort) {
+    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);             // S^T, dP^T: A, B K-major
+    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);              // dV, dK: A in TMEM, B MN-major
+    constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // dQ^T: A and B MN-major
+    if (!tc::mbar_wait(tc::smem_addr(&bar[B_KV]), item_count & 1, abort, kTimeoutNs)) return;
+    tc::tc_fence_after();
+    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V, sS = sbase + SM_S;
+    for (int s = 0; s < c.n_steps; ++s) {
+        const uint32_t ts = ts_base + s, st = ts & 1;
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts >> 1) & 1, abort, kTimeoutNs)) return;
+        tc::tc_fence_after();
+        const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
+        // S^T = K Q^T (overwrites P^T of the previous step: wait for the dV that read it)
+        if (s > 0) {
+            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DV]), (ts - 1) & 1, abort, kTimeoutNs)) return;
+            tc::tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
+            tc::mma_ss(tmem + TS, tc::sdesc_sw128(sK + oa, 16, 1024), tc::sdesc_sw128(sQ + ob, 16, 1024), id_st, k > 0);
+        }
+        tc::mma_commit(tc::smem_addr(&bar[B_S]));
+        // dP^T = V dO^T (overwrites dS^T of the previous step: wait for the dK that read it)
+        if (s > 0) {
+            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DK]), (ts - 1) & 1, abort, kTimeoutNs)) return;
+            tc::tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
+            tc::mma_ss(tmem + TDP, tc::sdesc_sw128(sV + oa, 16, 1024), tc::sdesc_sw128(sO + ob, 16, 1024), id_st, k > 0);
+        }
+        tc::mma_commit(tc::smem_addr(&bar[B_DP]));
+        // P^T, dS^T ready
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_SM]), ts & 1, abort, kTimeoutNs)) return;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+            tc::mma_ts(tmem + TDV, tmem + TS + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
+                       (s > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(tc::smem_addr(&bar[B_DV]));
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+            tc::mma_ts(tmem + TDK, tmem + TDP + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
+                       (s > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(tc::smem_addr(&bar[B_DK]));
+        // dQ^T = K^T dS^T (overwrites the previous step's dQ^T: wait until it was read out)
+        if (s > 0) {
+            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DQF]), (ts - 1) & 1, abort, kTimeoutNs)) return;
+            tc::tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+            tc::mma_ss(tmem + TDQ, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
+                       id_dq, k > 0);
+        tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
+        tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
+    }
+}
+
+// --------------------------------------------------------------- compute
+// Thread = one key row (TMEM lane) x 32 query columns of the step (group g).
+__device__ __forceinline__ bool compute_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, uint8_t* smem,
+                                             const uint64_t* bar, const StepInfo* info, uint32_t tmem,
+                                             const CUtensorMap* tdq, uint32_t ts_base, volatile int* abort) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = warp >> 2;                       // column group
+    const int kk = 32 * (warp & 3) + lane;         // key row in the tile == TMEM lane
+    const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+    const int kr = c.k0 + kk;
+    const bool key_ok = kk < c.kv_rows;
+    const float sl2 = a.scale_log2;
+    float* stg = reinterpret_cast<float*>(smem + SM_STG);
+    for (int s = 0; s < c.n_steps; ++s) {
+        const uint32_t ts = ts_base + s, st = ts & 1;
+        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts >> 1) & 1, abort, kTimeoutNs);
+        got = got && tc::mbar_wait(tc::smem_addr(&bar[B_S]), ts & 1, abort, kTimeoutNs);
+        got = got && tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
+        if (!named_and(1, 256, got)) return false;
+        tc::tc_fence_after();
+        uint32_t sr[32], dr[32];
+        tc::tmem_ld32(tmem + lb + TS + 32 * g, sr);
+        tc::tmem_ld32(tmem + lb + TDP + 32 * g, dr);
+        tc::tmem_ld_wait();
+        const StepInfo& inf = info[st];
+        const bool full = inf.full != 0;
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float p[2], ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int col = 32 * g + 2 * e + u;
+                float pv = ex2f(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -inf.lse2[col]));
+                if (!full && !(key_ok && span_sees(inf.span[col], kr))) pv = 0.f;
+                p[u] = pv;
+                ds[u] = pv * (__uint_as_float(dr[2 * e + u]) - inf.dsum[col]);
+            }
+            pp[e] = pack2(p[0], p[1]);
+            dd[e] = pack2(ds[0], ds[1]);
+        }
+        tc::tmem_st16(tmem + lb + TS + 16 * g, pp);
+        tc::tmem_st16(tmem + lb + TDP + 16 * g, dd);
+        {   // dS^T row kk, query columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
+            uint8_t* row = smem + SM_S + kk * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int chunk = (4 * g + q) ^ (kk & 7);
+                *reinterpret_cast<uint4*>(row + chunk * 16) =
+                    make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+            }
+        }
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_SM]));
+
+        // dQ^T of this step: lane = d, columns = query rows 32g..32g+31
+        got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ]), ts & 1, abort, kTimeoutNs);
+        if (!named_and(1, 256, got)) return false;
+        tc::tc_fence_after();
+        uint32_t qv[32];
+        tc::tmem_ld32(tmem + lb + TDQ + 32 * g, qv);
+        tc::tmem_ld_wait();
+        if (tid == 0) bulk_wait_read0();  // the previous reduce has read the staging tile
+        named_sync(1, 256);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) stg[(32 * g + e) * D + kk] = __uint_as_float(qv[e]) * a.scale;
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        named_sync(1, 256);
+        if (tid == 0) {
+            int h, p0, nrows;
+            step_rows(c, a, s, &h, &p0, &nrows);
+            tma_reduce_add_3d(tdq, sbase + SM_STG, 0, h, c.kt.doc_start + p0);
+            bulk_commit();
+            tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));
+        }
+    }
+    // dK (group 0) or dV (group 1) of this item: all MMAs are complete (the
+    // last dQ^T commit covered them)
+    const uint32_t src = g == 0 ? TDK : TDV;
+    __nv_bfloat16* dst = (g == 0 ? a.dk : a.dv) + (long long)kr * ((long long)a.Hk * D) + (long long)c.kvh * D;
+    const float mul = g == 0 ? a.scale : 1.f;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lb + src + 32 * q, v);
+        tc::tmem_ld_wait();
+        if (key_ok) {
+            uint4* o = reinterpret_cast<uint4*>(dst + 32 * q);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[e] = make_uint4(pack2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                  pack2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                  pack2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                  pack2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = tc::smem_addr(smem);
+    __shared__ __align__(8) uint64_t bar[B_COUNT];
+    __shared__ __align__(16) StepInfo info[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_item;
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        s_abort = 0;
+        tc::mbar_init(tc::smem_addr(&bar[B_KV]), 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 32);
+            tc::mbar_init(tc::smem_addr(&bar[B_QDE + s]), 1);
+        }
+        tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_DP]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_SM]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_DV]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_DK]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_DQ]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 9) {
+        tc::tmem_alloc(tc::smem_addr(&s_tmem), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_do);
+        tc::prefetch_tmap(&tm_dq);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort = &s_abort;
+    const int n_items = a.hdr->n_tiles * a.Hk;
+    uint32_t ts_base = 0, item_count = 0;
+    for (;;) {
+        __syncthreads();
+        if (tid == 0) s_item = *abort ? n_items : atomicAdd(&a.hdr->counter, 1);
+        __syncthreads();
+        const int item = s_item;
+        if (item >= n_items) break;
+        const ItemCtx c = decode(a, item);
+        if (warp == 8) {
+            load_item(c, a, sbase, bar, info, &tm_k, &tm_v, &tm_q, &tm_do, ts_base, abort);
+        } else if (warp == 9) {
+            if (lane == 0) issue_item(c, sbase, bar, tmem, ts_base, item_count, abort);
+        } else {
+            compute_item(c, a, sbase, smem, bar, info, tmem, &tm_dq, ts_base, abort);
+        }
+        ts_base += c.n_steps;
+        ++item_count;
+    }
+    if (tid == 0) bulk_wait0();  // every dq reduce has landed
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && s_abort) set_error(a.hdr, DEV_TIMEOUT, blockIdx.x);
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [rows, heads, D] tensor as a 3-D map (D, heads, rows) with (box_d, 1, box_rows) boxes.
+bool make_map(CUtensorMap* m, const void* base, bool f32, int heads, long long rows, int box_d, int box_rows,
+              CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int esz = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)heads * D * esz};
+    cuuint32_t box[3] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st) {
+    CUtensorMap mk, mv, mq, mdo, mdq;
+    if (!make_map(&mk, a.k, false, a.Hk, a.L, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, a.v, false, a.Hk, a.L, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mq, a.q, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mdo, a.dO, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mdq, a.dqacc, true, a.H, a.L, D, BQ, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    bwd_tc_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, a);
+    return cudaGetLastError();
+}
+
+}  // namespace bdlm
