@@ -19,12 +19,23 @@
 // dK and dV stay in TMEM for the whole item (no atomics: the item owns its
 // keys for all G heads) and are written once, as bf16, at the end.
 //
-// Warp roles (320 threads): warps 0-7 compute (two groups of 4 warps, one
-// TMEM lane = one key row; group g takes query columns 32g..32g+31 of a
-// step), warp 8 loads (TMA for K, V, Q, dO; plain loads for lse, D and the
-// query rows' key intervals), warp 9 owns TMEM and issues the MMAs.
+// Warp roles (448 threads):
+//   warps 0-7   P/dS groups: one TMEM lane = one key row; group g (warps
+//               4g..4g+3) takes query columns 32g..32g+31 of a step. The mask
+//               is analytic: for one key, the rows of a step that see it form
+//               one interval (later clean blocks / later corrupted blocks for a
+//               clean key, its own corrupted block for a corrupted key).
+//   warps 8-11  dq group: reads dQ^T (lane = d) out to the TMA reduce-add
+//               through a double-buffered staging tile, and writes dK and dV
+//               at the end of an item
+//   warp  12    loader: TMA for K, V, Q, dO; cp.async for lse and D; 3-stage
+//               ring for the per-step inputs
+//   warp  13    TMEM owner and MMA issuer (one thread). Per step s it issues
+//              S^T(s), dP^T(s), dQ^T(s-1), then dV(s) and dK(s) once P/dS(s)
+//              is ready, so dQ^T(s-1) overlaps the P/dS work of step s.
 // TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
-// dQ^T [384,448). Every mbarrier wait is bounded (2 s).
+// dQ^T double buffer [384,448) [448,512). dS^T in shared memory is double
+// buffered too. Every mbarrier wait is bounded (2 s).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -37,34 +48,35 @@ namespace {
 constexpr int D = 128;
 constexpr int BN = 128;  // keys per item
 constexpr int BQ = 64;   // query rows per step
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TDQ = 384;
+constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TDQ = 384;  // + 64 * buffer
+constexpr int kStages = 3;
 
 // dynamic shared memory (1024-aligned offsets)
 constexpr int kKV = BN * D * 2;     // 32 KB: K or V tile, two 64-column chunks of 16 KB
 constexpr int kQT = BQ * D * 2;     // 16 KB: Q or dO tile, two chunks of 8 KB
+constexpr int kST = BN * BQ * 2;    // 16 KB: dS^T [128 keys][64 rows] bf16, 128-byte swizzled rows
+constexpr int kHalfRows = BQ / 2;   // dq staging holds half a step: [32 rows][128] fp32
 constexpr int SM_K = 0;
 constexpr int SM_V = SM_K + kKV;
-constexpr int SM_Q = SM_V + kKV;          // + stage * kQT
-constexpr int SM_O = SM_Q + 2 * kQT;      // + stage * kQT
-constexpr int SM_S = SM_O + 2 * kQT;      // dS^T [128 keys][64 rows] bf16, 128-byte swizzled rows
-constexpr int SM_STG = SM_S + BN * BQ * 2;  // dq staging [64 rows][128] fp32
-constexpr int kSmemBytes = SM_STG + BQ * D * 4 + 1024;
+constexpr int SM_Q = SM_V + kKV;                // + stage * kQT
+constexpr int SM_O = SM_Q + kStages * kQT;      // + stage * kQT
+constexpr int SM_S = SM_O + kStages * kQT;      // + buffer * kST
+constexpr int kStg = kHalfRows * D * 4;  // 16 KB per staging buffer
+constexpr int SM_STG = SM_S + 2 * kST;     // + buffer * kStg
+constexpr int kSmemBytes = SM_STG + 2 * kStg + 1024;
 
 enum : int {
-    B_KV = 0, B_QDF = 1, B_QDE = 3, B_S = 5, B_DP = 6, B_SM = 7, B_DV = 8, B_DK = 9, B_DQ = 10, B_DQF = 11,
-    B_COUNT = 12
+    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_DV = 10, B_DK = 11, B_DQ = 12, B_DQF = 14,
+    B_COUNT = 16
 };
 
 struct StepInfo {
-    float lse2[BQ];  // lse * log2(e); +inf for rows without keys or beyond the step
+    float lse[BQ];   // lse of the step's rows (0 beyond the step; those rows are masked)
     float dsum[BQ];  // D = rowsum(dO * o)
-    Span span[BQ];
-    int full;        // every row sees every key of the tile
-    int pad[3];
 };
 
 struct ItemCtx {
@@ -94,6 +106,7 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // Barrier over the n threads of named barrier `id` that also ANDs a predicate,
@@ -144,6 +157,14 @@ __device__ __forceinline__ void step_rows(const ItemCtx& c, const BwdArgs& a, in
 }
 
 // ---------------------------------------------------------------- loader
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0) : "memory");
+}
+// arrive on `bar` once all earlier cp.async of this thread have landed
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, const uint64_t* bar,
                                           StepInfo* info, const CUtensorMap* tk, const CUtensorMap* tv,
                                           const CUtensorMap* tq, const CUtensorMap* tdo, uint32_t ts_base,
@@ -158,8 +179,8 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
         }
     }
     for (int s = 0; s < c.n_steps; ++s) {
-        const uint32_t ts = ts_base + s, st = ts & 1;
-        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + st]), ((ts >> 1) & 1) ^ 1, abort, kTimeoutNs);
+        const uint32_t ts = ts_base + s, st = ts % kStages, ph = (ts / kStages) & 1;
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + st]), ph ^ 1, abort, kTimeoutNs);
         if (!__all_sync(0xffffffffu, got)) return;
         int h, p0, nrows;
         step_rows(c, a, s, &h, &p0, &nrows);
@@ -173,48 +194,53 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
             }
         }
         StepInfo& inf = info[st];
-        const Tile qt{c.kt.doc_start, c.kt.n, p0, nrows};
-        bool rowfull = true;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int r = 2 * lane + u;
-            const Span sp = row_span(a.lay, qt, r);
-            float l2 = INFINITY, dd = 0.f;
-            if (r < nrows) {
-                const float lse = __ldg(a.lse + (long long)h * a.L + qr0 + r);
-                l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
-                dd = __ldg(a.Dsum + (long long)h * a.L + qr0 + r);
-            }
-            inf.lse2[r] = l2;
-            inf.dsum[r] = dd;
-            inf.span[r] = sp;
-            rowfull = rowfull && r < nrows && sp.p_lo <= c.k0 && c.k0 + BN <= sp.p_hi;
+            const bool ok = r < nrows;
+            const long long gi = (long long)h * a.L + qr0 + (ok ? r : 0);
+            cp_async4(tc::smem_addr(&inf.lse[r]), a.lse + gi, ok);
+            cp_async4(tc::smem_addr(&inf.dsum[r]), a.Dsum + gi, ok);
         }
-        const bool full = __all_sync(0xffffffffu, rowfull) && c.kv_rows == BN;
-        if (lane == 0) inf.full = full ? 1 : 0;
+        cp_async_arrive(bf);
         tc::mbar_arrive(bf);
     }
 }
 
 // ------------------------------------------------------------------- MMA
+__device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t parity, volatile int* abort) {
+    if (!tc::mbar_wait(tc::smem_addr(&bar[i]), parity, abort, kTimeoutNs)) return false;
+    tc::tc_fence_after();
+    return true;
+}
+
+__device__ __forceinline__ void issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
+                                         volatile int* abort, bool* ok) {
+    constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
+    const uint32_t b = ts & 1;
+    // the dQ^T buffer of step ts - 2 must have been read out
+    if (s >= 2 && !mma_wait(bar, B_DQF + b, ((ts >> 1) - 1) & 1, abort)) { *ok = false; return; }
+    const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + b * kST;
+#pragma unroll
+    for (int k = 0; k < BN / 16; ++k)
+        tc::mma_ss(tmem + TDQ + 64 * b, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
+                   id_dq, k > 0);
+    tc::mma_commit(tc::smem_addr(&bar[B_DQ + b]));
+}
+
 __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
                                            uint32_t ts_base, uint32_t item_count, volatile int* abort) {
-    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);             // S^T, dP^T: A, B K-major
-    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);              // dV, dK: A in TMEM, B MN-major
-    constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // dQ^T: A and B MN-major
-    if (!tc::mbar_wait(tc::smem_addr(&bar[B_KV]), item_count & 1, abort, kTimeoutNs)) return;
-    tc::tc_fence_after();
-    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V, sS = sbase + SM_S;
+    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // S^T, dP^T: A, B K-major
+    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);   // dV, dK: A in TMEM, B MN-major
+    if (!mma_wait(bar, B_KV, item_count & 1, abort)) return;
+    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V;
+    bool ok = true;
     for (int s = 0; s < c.n_steps; ++s) {
-        const uint32_t ts = ts_base + s, st = ts & 1;
-        if (!tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts >> 1) & 1, abort, kTimeoutNs)) return;
-        tc::tc_fence_after();
+        const uint32_t ts = ts_base + s, st = ts % kStages;
+        if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return;
         const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
         // S^T = K Q^T (overwrites P^T of the previous step: wait for the dV that read it)
-        if (s > 0) {
-            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DV]), (ts - 1) & 1, abort, kTimeoutNs)) return;
-            tc::tc_fence_after();
-        }
+        if (s > 0 && !mma_wait(bar, B_DV, (ts - 1) & 1, abort)) return;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
@@ -222,19 +248,19 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
         }
         tc::mma_commit(tc::smem_addr(&bar[B_S]));
         // dP^T = V dO^T (overwrites dS^T of the previous step: wait for the dK that read it)
-        if (s > 0) {
-            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DK]), (ts - 1) & 1, abort, kTimeoutNs)) return;
-            tc::tc_fence_after();
-        }
+        if (s > 0 && !mma_wait(bar, B_DK, (ts - 1) & 1, abort)) return;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
             tc::mma_ss(tmem + TDP, tc::sdesc_sw128(sV + oa, 16, 1024), tc::sdesc_sw128(sO + ob, 16, 1024), id_st, k > 0);
         }
         tc::mma_commit(tc::smem_addr(&bar[B_DP]));
-        // P^T, dS^T ready
-        if (!tc::mbar_wait(tc::smem_addr(&bar[B_SM]), ts & 1, abort, kTimeoutNs)) return;
-        tc::tc_fence_after();
+        // dQ^T of the previous step fills the gap while P/dS of this step is computed
+        if (s > 0) {
+            issue_dq(sbase, bar, tmem, ts - 1, s - 1, abort, &ok);
+            if (!ok) return;
+        }
+        if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
             tc::mma_ts(tmem + TDV, tmem + TS + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
@@ -245,117 +271,165 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
             tc::mma_ts(tmem + TDK, tmem + TDP + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
                        (s > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(tc::smem_addr(&bar[B_DK]));
-        // dQ^T = K^T dS^T (overwrites the previous step's dQ^T: wait until it was read out)
-        if (s > 0) {
-            if (!tc::mbar_wait(tc::smem_addr(&bar[B_DQF]), (ts - 1) & 1, abort, kTimeoutNs)) return;
-            tc::tc_fence_after();
-        }
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-            tc::mma_ss(tmem + TDQ, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
-                       id_dq, k > 0);
-        tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
         tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
     }
+    if (c.n_steps > 0) issue_dq(sbase, bar, tmem, ts_base + c.n_steps - 1, c.n_steps - 1, abort, &ok);
 }
 
-// --------------------------------------------------------------- compute
-// Thread = one key row (TMEM lane) x 32 query columns of the step (group g).
-__device__ __forceinline__ bool compute_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, uint8_t* smem,
-                                             const uint64_t* bar, const StepInfo* info, uint32_t tmem,
-                                             const CUtensorMap* tdq, uint32_t ts_base, volatile int* abort) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = warp >> 2;                       // column group
-    const int kk = 32 * (warp & 3) + lane;         // key row in the tile == TMEM lane
+// ------------------------------------------------------------ P/dS group
+// Query columns [lo, lo + len) of a step whose rows see key row kk of the
+// tile (doc positions: keys from the tile, rows p0 .. p0 + nrows - 1, one
+// half of one document). For a clean key of block b: clean rows of blocks
+// >= b and corrupted rows of blocks > b; for a corrupted key of block b: the
+// corrupted rows of block b.
+__device__ __forceinline__ void visible_cols(const ItemCtx& c, int B, int kk, int p0, int nrows, int* lo, int* len) {
+    const int n = c.kt.n;
+    const int kc = c.kt.pos0 + kk;
+    int a, b;
+    if (kk >= c.kv_rows) {
+        a = 0;
+        b = 0;
+    } else if (kc < n) {
+        const int bk = kc / B;
+        a = p0 < n ? bk * B - p0 : n + (bk + 1) * B - p0;
+        b = nrows;
+    } else {
+        const int bk = (kc - n) / B;
+        a = n + bk * B - p0;
+        b = a + B;
+    }
+    a = imax(a, 0);
+    b = imin(b, nrows);
+    *lo = a;
+    *len = imax(b - a, 0);
+}
+
+// Thread = one key row (TMEM lane) x query columns 32g .. 32g + 31.
+__device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uint8_t* smem, const uint64_t* bar,
+                                         const StepInfo* info, uint32_t tmem, uint32_t ts_base, volatile int* abort) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = warp >> 2;
+    const int kk = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-    const int kr = c.k0 + kk;
-    const bool key_ok = kk < c.kv_rows;
     const float sl2 = a.scale_log2;
-    float* stg = reinterpret_cast<float*>(smem + SM_STG);
+    constexpr float kLog2e = 1.4426950408889634f;
     for (int s = 0; s < c.n_steps; ++s) {
-        const uint32_t ts = ts_base + s, st = ts & 1;
-        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts >> 1) & 1, abort, kTimeoutNs);
+        const uint32_t ts = ts_base + s, st = ts % kStages;
+        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts / kStages) & 1, abort, kTimeoutNs);
         got = got && tc::mbar_wait(tc::smem_addr(&bar[B_S]), ts & 1, abort, kTimeoutNs);
         got = got && tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
-        if (!named_and(1, 256, got)) return false;
+        if (!__all_sync(0xffffffffu, got)) return;
         tc::tc_fence_after();
         uint32_t sr[32], dr[32];
         tc::tmem_ld32(tmem + lb + TS + 32 * g, sr);
         tc::tmem_ld32(tmem + lb + TDP + 32 * g, dr);
+        int h, p0, nrows;
+        step_rows(c, a, s, &h, &p0, &nrows);
+        int lo, len;
+        visible_cols(c, a.lay.B, kk, p0, nrows, &lo, &len);
+        lo -= 32 * g;  // relative to this group's first column
+        const float4* lse4 = reinterpret_cast<const float4*>(info[st].lse + 32 * g);
+        const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 32 * g);
         tc::tmem_ld_wait();
-        const StepInfo& inf = info[st];
-        const bool full = inf.full != 0;
         uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            float p[2], ds[2];
+        for (int q = 0; q < 8; ++q) {
+            const float4 l4 = lse4[q], d4 = ds4[q];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float p[4], ds[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int col = 32 * g + 2 * e + u;
-                float pv = ex2f(fmaf(__uint_as_float(sr[2 * e + u]), sl2, -inf.lse2[col]));
-                if (!full && !(key_ok && span_sees(inf.span[col], kr))) pv = 0.f;
+            for (int u = 0; u < 4; ++u) {
+                const int col = 4 * q + u;
+                float pv = ex2f(fmaf(__uint_as_float(sr[col]), sl2, -lv[u] * kLog2e));
+                pv = (unsigned)(col - lo) < (unsigned)len ? pv : 0.f;
                 p[u] = pv;
-                ds[u] = pv * (__uint_as_float(dr[2 * e + u]) - inf.dsum[col]);
+                ds[u] = pv * (__uint_as_float(dr[col]) - dv[u]);
             }
-            pp[e] = pack2(p[0], p[1]);
-            dd[e] = pack2(ds[0], ds[1]);
+            pp[2 * q] = pack2(p[0], p[1]);
+            pp[2 * q + 1] = pack2(p[2], p[3]);
+            dd[2 * q] = pack2(ds[0], ds[1]);
+            dd[2 * q + 1] = pack2(ds[2], ds[3]);
         }
         tc::tmem_st16(tmem + lb + TS + 16 * g, pp);
         tc::tmem_st16(tmem + lb + TDP + 16 * g, dd);
-        {   // dS^T row kk, query columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
-            uint8_t* row = smem + SM_S + kk * 128;
+        {   // dS^T row kk, columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
+            uint8_t* srow = smem + SM_S + (ts & 1) * kST + kk * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int chunk = (4 * g + q) ^ (kk & 7);
-                *reinterpret_cast<uint4*>(row + chunk * 16) =
-                    make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                *reinterpret_cast<uint4*>(srow + chunk * 16) = make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
             }
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(tc::smem_addr(&bar[B_SM]));
+    }
+}
 
-        // dQ^T of this step: lane = d, columns = query rows 32g..32g+31
-        got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ]), ts & 1, abort, kTimeoutNs);
-        if (!named_and(1, 256, got)) return false;
+// -------------------------------------------------------------- dq group
+// Thread = one head-dim lane d of dQ^T (TMEM lane) x 64 query columns; the
+// step's dq goes out as two TMA reduce-adds of 32 rows through two staging
+// buffers. At the end of the item it writes dK and dV (thread = key row).
+__device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, uint8_t* smem,
+                                        const uint64_t* bar, uint32_t tmem, const CUtensorMap* tdq, uint32_t ts_base,
+                                        volatile int* abort) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int dl = 32 * (warp & 3) + lane;  // d index == TMEM lane
+    const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+    const bool leader = tid == 256;
+    for (int s = 0; s < c.n_steps; ++s) {
+        const uint32_t ts = ts_base + s, b = ts & 1;
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ + b]), (ts >> 1) & 1, abort, kTimeoutNs);
+        if (!named_and(2, 128, got)) return false;
         tc::tc_fence_after();
-        uint32_t qv[32];
-        tc::tmem_ld32(tmem + lb + TDQ + 32 * g, qv);
+        int h, p0, nrows;
+        step_rows(c, a, s, &h, &p0, &nrows);
+        uint32_t qv[2][32];
+        tc::tmem_ld32(tmem + lb + TDQ + 64 * b, qv[0]);
+        tc::tmem_ld32(tmem + lb + TDQ + 64 * b + 32, qv[1]);
         tc::tmem_ld_wait();
-        if (tid == 0) bulk_wait_read0();  // the previous reduce has read the staging tile
-        named_sync(1, 256);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) stg[(32 * g + e) * D + kk] = __uint_as_float(qv[e]) * a.scale;
-        tc::fence_proxy_async_smem();
         tc::tc_fence_before();
-        named_sync(1, 256);
-        if (tid == 0) {
-            int h, p0, nrows;
-            step_rows(c, a, s, &h, &p0, &nrows);
-            tma_reduce_add_3d(tdq, sbase + SM_STG, 0, h, c.kt.doc_start + p0);
-            bulk_commit();
-            tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            // staging buffer `half` was last read by the reduce issued one step ago
+            if (leader) bulk_wait_read1();
+            named_sync(2, 128);
+            float* stg = reinterpret_cast<float*>(smem + SM_STG + half * kStg);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) stg[e * D + dl] = __uint_as_float(qv[half][e]) * a.scale;
+            tc::fence_proxy_async_smem();
+            named_sync(2, 128);
+            if (leader) {
+                tma_reduce_add_3d(tdq, sbase + SM_STG + half * kStg, 0, h, c.kt.doc_start + p0 + kHalfRows * half);
+                bulk_commit();
+                if (half == 1) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF + b]));
+            }
         }
     }
-    // dK (group 0) or dV (group 1) of this item: all MMAs are complete (the
-    // last dQ^T commit covered them)
-    const uint32_t src = g == 0 ? TDK : TDV;
-    __nv_bfloat16* dst = (g == 0 ? a.dk : a.dv) + (long long)kr * ((long long)a.Hk * D) + (long long)c.kvh * D;
-    const float mul = g == 0 ? a.scale : 1.f;
+    // dK and dV: the last dQ^T commit covered every MMA of the item
+    const int kk = dl;
+    const bool key_ok = kk < c.kv_rows;
+    const long long rowoff = (long long)(c.k0 + kk) * ((long long)a.Hk * D) + (long long)c.kvh * D;
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+        const uint32_t src = which == 0 ? TDK : TDV;
+        __nv_bfloat16* dst = (which == 0 ? a.dk : a.dv) + rowoff;
+        const float mul = which == 0 ? a.scale : 1.f;
 #pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + lb + src + 32 * q, v);
-        tc::tmem_ld_wait();
-        if (key_ok) {
-            uint4* o = reinterpret_cast<uint4*>(dst + 32 * q);
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem + lb + src + 32 * q, v);
+            tc::tmem_ld_wait();
+            if (key_ok) {
+                uint4* o = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o[e] = make_uint4(pack2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                                  pack2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                                  pack2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                                  pack2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+                for (int e = 0; e < 4; ++e)
+                    o[e] = make_uint4(pack2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                      pack2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                      pack2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                      pack2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+            }
         }
     }
     return true;
@@ -370,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = tc::smem_addr(smem);
     __shared__ __align__(8) uint64_t bar[B_COUNT];
-    __shared__ __align__(16) StepInfo info[2];
+    __shared__ __align__(16) StepInfo info[kStages];
     __shared__ uint32_t s_tmem;
     __shared__ int s_item;
     __shared__ int s_abort;
@@ -379,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         s_abort = 0;
         tc::mbar_init(tc::smem_addr(&bar[B_KV]), 1);
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 32);
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 64);  // 32 lanes x (stores + cp.async)
             tc::mbar_init(tc::smem_addr(&bar[B_QDE + s]), 1);
         }
         tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
@@ -388,15 +462,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(tc::smem_addr(&bar[B_SM]), 256);
         tc::mbar_init(tc::smem_addr(&bar[B_DV]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_DK]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_DQ]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tc::smem_addr(&bar[B_DQ + b]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_DQF + b]), 1);
+        }
         tc::fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tc::tmem_alloc(tc::smem_addr(&s_tmem), kTmemCols);
         tc::tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         tc::prefetch_tmap(&tm_k);
         tc::prefetch_tmap(&tm_v);
         tc::prefetch_tmap(&tm_q);
@@ -417,20 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int item = s_item;
         if (item >= n_items) break;
         const ItemCtx c = decode(a, item);
-        if (warp == 8) {
+        if (warp == 12) {
             load_item(c, a, sbase, bar, info, &tm_k, &tm_v, &tm_q, &tm_do, ts_base, abort);
-        } else if (warp == 9) {
+        } else if (warp == 13) {
             if (lane == 0) issue_item(c, sbase, bar, tmem, ts_base, item_count, abort);
+        } else if (warp < 8) {
+            pds_item(c, a, smem, bar, info, tmem, ts_base, abort);
         } else {
-            compute_item(c, a, sbase, smem, bar, info, tmem, &tm_dq, ts_base, abort);
+            dq_item(c, a, sbase, smem, bar, tmem, &tm_dq, ts_base, abort);
         }
         ts_base += c.n_steps;
         ++item_count;
     }
-    if (tid == 0) bulk_wait0();  // every dq reduce has landed
+    if (tid == 256) bulk_wait0();  // every dq reduce has landed
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
@@ -479,7 +557,7 @@ cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st) {
         !make_map(&mv, a.v, false, a.Hk, a.L, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mq, a.q, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mdo, a.dO, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdq, a.dqacc, true, a.H, a.L, D, BQ, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map(&mdq, a.dqacc, true, a.H, a.L, D, kHalfRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
