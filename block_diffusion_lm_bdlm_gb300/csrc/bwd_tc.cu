@@ -9,10 +9,10 @@
 //   S^T  = K Q^T          (M 128 keys, N 64 rows, K = d)      -> TMEM
 //   dP^T = V dO^T                                              -> TMEM
 //   P^T  = exp2(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D)
-//          (compute warps; P^T and dS^T go back to TMEM as bf16, dS^T also
-//          to shared memory)
+//          (compute warps; P^T goes to its own TMEM columns as bf16, dS^T to
+//          shared memory, where it is both dK's A and dQ^T's B operand)
 //   dV  += P^T dO         (A from TMEM)                        -> TMEM
-//   dK  += dS^T Q         (A from TMEM)                        -> TMEM
+//   dK  += dS^T Q         (A from shared memory)               -> TMEM
 //   dQ^T = K^T dS^T       (M = d, N 64 rows, K 128 keys)       -> TMEM
 //          read out, scaled, staged in shared memory and added into the fp32
 //          dq accumulator with one TMA reduce-add per step.
@@ -34,8 +34,11 @@
 //              S^T(s), dP^T(s), dQ^T(s-1), then dV(s) and dK(s) once P/dS(s)
 //              is ready, so dQ^T(s-1) overlaps the P/dS work of step s.
 // TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
-// dQ^T double buffer [384,448) [448,512). dS^T in shared memory is double
-// buffered too. Every mbarrier wait is bounded (2 s).
+// P^T [384,416) | dQ^T [416,480). dS^T in shared memory is double buffered.
+// Because P^T and dS^T do not alias S^T and dP^T, the only per-step
+// handshake the MMA thread waits for is P/dS; tcgen05 commit order covers
+// the rest (an MMA's commit also covers every MMA issued before it).
+// Every mbarrier wait is bounded (2 s).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -52,7 +55,7 @@ constexpr int kThreads = 448;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TDQ = 384;  // + 64 * buffer
+constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TP = 384, TDQ = 416;
 constexpr int kStages = 3;
 
 // dynamic shared memory (1024-aligned offsets)
@@ -217,21 +220,20 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
 __device__ __forceinline__ void issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
                                          volatile int* abort, bool* ok) {
     constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
-    const uint32_t b = ts & 1;
-    // the dQ^T buffer of step ts - 2 must have been read out
-    if (s >= 2 && !mma_wait(bar, B_DQF + b, ((ts >> 1) - 1) & 1, abort)) { *ok = false; return; }
-    const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + b * kST;
+    // dQ^T of the previous step must have been read out of TMEM
+    if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) { *ok = false; return; }
+    const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + (ts & 1) * kST;
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k)
-        tc::mma_ss(tmem + TDQ + 64 * b, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
+        tc::mma_ss(tmem + TDQ, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
                    id_dq, k > 0);
-    tc::mma_commit(tc::smem_addr(&bar[B_DQ + b]));
+    tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
 }
 
 __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
                                            uint32_t ts_base, uint32_t item_count, volatile int* abort) {
     constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // S^T, dP^T: A, B K-major
-    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);   // dV, dK: A in TMEM, B MN-major
+    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);   // dV, dK: A K-major (TMEM / smem), B MN-major
     if (!mma_wait(bar, B_KV, item_count & 1, abort)) return;
     const uint32_t sK = sbase + SM_K, sV = sbase + SM_V;
     bool ok = true;
@@ -239,16 +241,15 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
         const uint32_t ts = ts_base + s, st = ts % kStages;
         if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return;
         const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
-        // S^T = K Q^T (overwrites P^T of the previous step: wait for the dV that read it)
-        if (s > 0 && !mma_wait(bar, B_DV, (ts - 1) & 1, abort)) return;
+        // S^T = K Q^T. P/dS of the previous step has read S^T and dP^T (the
+        // MMAs of that step were issued after its B_SM), and P^T lives apart.
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
             tc::mma_ss(tmem + TS, tc::sdesc_sw128(sK + oa, 16, 1024), tc::sdesc_sw128(sQ + ob, 16, 1024), id_st, k > 0);
         }
         tc::mma_commit(tc::smem_addr(&bar[B_S]));
-        // dP^T = V dO^T (overwrites dS^T of the previous step: wait for the dK that read it)
-        if (s > 0 && !mma_wait(bar, B_DK, (ts - 1) & 1, abort)) return;
+        // dP^T = V dO^T
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
@@ -261,16 +262,16 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
             if (!ok) return;
         }
         if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
+        // dV += P^T dO (P^T in TMEM); dK += dS^T Q (dS^T in shared memory, K-major)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDV, tmem + TS + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
+            tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
                        (s > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(tc::smem_addr(&bar[B_DV]));
+        const uint32_t sS = sbase + SM_S + (ts & 1) * kST;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDK, tmem + TDP + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
-                       (s > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(tc::smem_addr(&bar[B_DK]));
+            tc::mma_ss(tmem + TDK, tc::sdesc_sw128(sS + 32 * k, 16, 1024), tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024),
+                       id_kv, (s > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
     }
     if (c.n_steps > 0) issue_dq(sbase, bar, tmem, ts_base + c.n_steps - 1, c.n_steps - 1, abort, &ok);
@@ -350,8 +351,7 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
             dd[2 * q] = pack2(ds[0], ds[1]);
             dd[2 * q + 1] = pack2(ds[2], ds[3]);
         }
-        tc::tmem_st16(tmem + lb + TS + 16 * g, pp);
-        tc::tmem_st16(tmem + lb + TDP + 16 * g, dd);
+        tc::tmem_st16(tmem + lb + TP + 16 * g, pp);
         {   // dS^T row kk, columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
             uint8_t* srow = smem + SM_S + (ts & 1) * kST + kk * 128;
 #pragma unroll
@@ -379,15 +379,15 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
     const bool leader = tid == 256;
     for (int s = 0; s < c.n_steps; ++s) {
-        const uint32_t ts = ts_base + s, b = ts & 1;
-        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ + b]), (ts >> 1) & 1, abort, kTimeoutNs);
+        const uint32_t ts = ts_base + s;
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ]), ts & 1, abort, kTimeoutNs);
         if (!named_and(2, 128, got)) return false;
         tc::tc_fence_after();
         int h, p0, nrows;
         step_rows(c, a, s, &h, &p0, &nrows);
         uint32_t qv[2][32];
-        tc::tmem_ld32(tmem + lb + TDQ + 64 * b, qv[0]);
-        tc::tmem_ld32(tmem + lb + TDQ + 64 * b + 32, qv[1]);
+        tc::tmem_ld32(tmem + lb + TDQ, qv[0]);
+        tc::tmem_ld32(tmem + lb + TDQ + 32, qv[1]);
         tc::tmem_ld_wait();
         tc::tc_fence_before();
 #pragma unroll
@@ -403,7 +403,7 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
             if (leader) {
                 tma_reduce_add_3d(tdq, sbase + SM_STG + half * kStg, 0, h, c.kt.doc_start + p0 + kHalfRows * half);
                 bulk_commit();
-                if (half == 1) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF + b]));
+                if (half == 1) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));
             }
         }
     }
