@@ -28,7 +28,7 @@
 //   warps 8-11  dq group: reads dQ^T (lane = d) out to the TMA reduce-add
 //               through a double-buffered staging tile, and writes dK and dV
 //               at the end of an item
-//   warp  12    loader: TMA for K, V, Q, dO; cp.async for lse and D; 3-stage
+//   warp  12    loader: TMA for K, V, Q, dO; plain loads for lse and D; 3-stage
 //               ring for the per-step inputs
 //   warp  13    TMEM owner and MMA issuer (one thread). Per step s it issues
 //              S^T(s), dP^T(s), dQ^T(s-1), then dV(s) and dK(s) once P/dS(s)
@@ -78,7 +78,7 @@ enum : int {
 };
 
 struct StepInfo {
-    float lse[BQ];   // lse of the step's rows (0 beyond the step; those rows are masked)
+    float nl2[BQ];   // -lse * log2(e) of the step's rows (0 beyond the step; those rows are masked)
     float dsum[BQ];  // D = rowsum(dO * o)
 };
 
@@ -108,7 +108,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
@@ -160,14 +159,6 @@ __device__ __forceinline__ void step_rows(const ItemCtx& c, const BwdArgs& a, in
 }
 
 // ---------------------------------------------------------------- loader
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0) : "memory");
-}
-// arrive on `bar` once all earlier cp.async of this thread have landed
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, const uint64_t* bar,
                                           StepInfo* info, const CUtensorMap* tk, const CUtensorMap* tv,
                                           const CUtensorMap* tq, const CUtensorMap* tdo, uint32_t ts_base,
@@ -196,16 +187,21 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
                 tc::tma_load_3d(sbase + SM_O + st * kQT + ch * (kQT / 2), tdo, bf, 64 * ch, h, qr0);
             }
         }
+        // lse and D: plain loads (the loader runs steps ahead of the MMAs),
+        // stored pre-scaled so that P/dS spends one FFMA per element before exp2
         StepInfo& inf = info[st];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int r = 2 * lane + u;
-            const bool ok = r < nrows;
-            const long long gi = (long long)h * a.L + qr0 + (ok ? r : 0);
-            cp_async4(tc::smem_addr(&inf.lse[r]), a.lse + gi, ok);
-            cp_async4(tc::smem_addr(&inf.dsum[r]), a.Dsum + gi, ok);
+            float nl2 = 0.f, dd = 0.f;
+            if (r < nrows) {
+                const long long gi = (long long)h * a.L + qr0 + r;
+                nl2 = -__ldg(a.lse + gi) * 1.4426950408889634f;
+                dd = __ldg(a.Dsum + gi);
+            }
+            inf.nl2[r] = nl2;
+            inf.dsum[r] = dd;
         }
-        cp_async_arrive(bf);
         tc::mbar_arrive(bf);
     }
 }
@@ -278,33 +274,6 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
 }
 
 // ------------------------------------------------------------ P/dS group
-// Query columns [lo, lo + len) of a step whose rows see key row kk of the
-// tile (doc positions: keys from the tile, rows p0 .. p0 + nrows - 1, one
-// half of one document). For a clean key of block b: clean rows of blocks
-// >= b and corrupted rows of blocks > b; for a corrupted key of block b: the
-// corrupted rows of block b.
-__device__ __forceinline__ void visible_cols(const ItemCtx& c, int B, int kk, int p0, int nrows, int* lo, int* len) {
-    const int n = c.kt.n;
-    const int kc = c.kt.pos0 + kk;
-    int a, b;
-    if (kk >= c.kv_rows) {
-        a = 0;
-        b = 0;
-    } else if (kc < n) {
-        const int bk = kc / B;
-        a = p0 < n ? bk * B - p0 : n + (bk + 1) * B - p0;
-        b = nrows;
-    } else {
-        const int bk = (kc - n) / B;
-        a = n + bk * B - p0;
-        b = a + B;
-    }
-    a = imax(a, 0);
-    b = imin(b, nrows);
-    *lo = a;
-    *len = imax(b - a, 0);
-}
-
 // Thread = one key row (TMEM lane) x query columns 32g .. 32g + 31.
 __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uint8_t* smem, const uint64_t* bar,
                                          const StepInfo* info, uint32_t tmem, uint32_t ts_base, volatile int* abort) {
@@ -313,9 +282,33 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
     const int kk = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
+    // Rows (document positions) that see this thread's key, per half: a clean
+    // key of block b is seen by clean rows of blocks >= b and corrupted rows of
+    // blocks > b; a corrupted key only by the corrupted rows of its block.
+    const int n = c.kt.n, B = a.lay.B, kc = c.kt.pos0 + kk;
+    int A0 = 0, A1 = 0, C0 = 0, C1 = 0;
+    if (kk < c.kv_rows) {
+        if (kc < n) {
+            const int bk = kc / B;
+            A0 = bk * B;
+            A1 = n;
+            C0 = n + (bk + 1) * B;
+            C1 = 2 * n;
+        } else {
+            C0 = n + ((kc - n) / B) * B;
+            C1 = C0 + B;
+        }
+    }
+    int rem = 0;  // step index within the current query head
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
+        const int p0 = rem < c.na ? c.ra_lo + rem * BQ : c.rb_lo + (rem - c.na) * BQ;
+        const int nrows = imin(BQ, (rem < c.na ? c.ra_hi : c.rb_hi) - p0);
+        if (++rem == c.per_head) rem = 0;
+        const int lo = imax((p0 < n ? A0 : C0) - p0, 0) - 32 * g;  // relative to this group's first column
+        const int hi = imin((p0 < n ? A1 : C1) - p0, nrows) - 32 * g;
+        const int len = imax(hi - lo, 0);
+        const bool all_visible = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
         bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts / kStages) & 1, abort, kTimeoutNs);
         got = got && tc::mbar_wait(tc::smem_addr(&bar[B_S]), ts & 1, abort, kTimeoutNs);
         got = got && tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
@@ -324,12 +317,7 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         uint32_t sr[32], dr[32];
         tc::tmem_ld32(tmem + lb + TS + 32 * g, sr);
         tc::tmem_ld32(tmem + lb + TDP + 32 * g, dr);
-        int h, p0, nrows;
-        step_rows(c, a, s, &h, &p0, &nrows);
-        int lo, len;
-        visible_cols(c, a.lay.B, kk, p0, nrows, &lo, &len);
-        lo -= 32 * g;  // relative to this group's first column
-        const float4* lse4 = reinterpret_cast<const float4*>(info[st].lse + 32 * g);
+        const float4* lse4 = reinterpret_cast<const float4*>(info[st].nl2 + 32 * g);
         const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 32 * g);
         tc::tmem_ld_wait();
         uint32_t pp[16], dd[16];
@@ -341,8 +329,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int col = 4 * q + u;
-                float pv = ex2f(fmaf(__uint_as_float(sr[col]), sl2, -lv[u] * kLog2e));
-                pv = (unsigned)(col - lo) < (unsigned)len ? pv : 0.f;
+                float pv = ex2f(fmaf(__uint_as_float(sr[col]), sl2, lv[u]));
+                if (!all_visible) pv = (unsigned)(col - lo) < (unsigned)len ? pv : 0.f;
                 p[u] = pv;
                 ds[u] = pv * (__uint_as_float(dr[col]) - dv[u]);
             }
@@ -454,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 0;
         tc::mbar_init(tc::smem_addr(&bar[B_KV]), 1);
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 64);  // 32 lanes x (stores + cp.async)
+            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 32);  // the loader's 32 lanes, after their stores
             tc::mbar_init(tc::smem_addr(&bar[B_QDE + s]), 1);
         }
         tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
