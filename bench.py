@@ -356,17 +356,22 @@ def end_to_end(step, x, flops, args, world, dev):
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
     e2e_steps = max(1, min(args.steps, 3))
+
+    def one_step():
+        for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
+            t.copy_(h, non_blocking=True)
+        step.run()
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    one_step()  # untimed: the first use of freshly pinned host buffers is slow
     torch.cuda.synchronize()
     barrier(world, dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(e2e_steps):
-        for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
-            t.copy_(h, non_blocking=True)
-        step.run()
-        for h, t in zip(h_out, outs):
-            h.copy_(t, non_blocking=True)
+        one_step()
     e1.record()
     torch.cuda.synchronize()
     barrier(world, dev)

@@ -321,23 +321,25 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 32 * g);
         tc::tmem_ld_wait();
         uint32_t pp[16], dd[16];
+        const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const float4 l4 = lse4[q], d4 = ds4[q];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float p[4], ds[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int col = 4 * q + u;
-                float pv = ex2f(fmaf(__uint_as_float(sr[col]), sl2, lv[u]));
-                if (!all_visible) pv = (unsigned)(col - lo) < (unsigned)len ? pv : 0.f;
-                p[u] = pv;
-                ds[u] = pv * (__uint_as_float(dr[col]) - dv[u]);
+            for (int u = 0; u < 2; ++u) {
+                const int col = 4 * q + 2 * u;
+                const float2 nl = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+                const float2 dsum = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                const float2 x = tc::fma2(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sl2x2, nl);
+                float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+                if (!all_visible) {
+                    p.x = (unsigned)(col - lo) < (unsigned)len ? p.x : 0.f;
+                    p.y = (unsigned)(col + 1 - lo) < (unsigned)len ? p.y : 0.f;
+                }
+                const float2 ds = tc::mul2(p, tc::sub2(make_float2(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), dsum));
+                pp[2 * q + u] = pack2(p.x, p.y);
+                dd[2 * q + u] = pack2(ds.x, ds.y);
             }
-            pp[2 * q] = pack2(p[0], p[1]);
-            pp[2 * q + 1] = pack2(p[2], p[3]);
-            dd[2 * q] = pack2(ds[0], ds[1]);
-            dd[2 * q + 1] = pack2(ds[2], ds[3]);
         }
         tc::tmem_st16(tmem + lb + TP + 16 * g, pp);
         {   // dS^T row kk, columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
