@@ -9,10 +9,10 @@
 //   S^T  = K Q^T          (M 128 keys, N 64 rows, K = d)      -> TMEM
 //   dP^T = V dO^T                                              -> TMEM
 //   P^T  = exp2(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D)
-//          (compute warps; P^T goes to its own TMEM columns as bf16, dS^T to
-//          shared memory, where it is both dK's A and dQ^T's B operand)
+//          (compute warps; P^T and dS^T go to their own TMEM columns as bf16
+//          for dV and dK, and dS^T also to shared memory for dQ^T)
 //   dV  += P^T dO         (A from TMEM)                        -> TMEM
-//   dK  += dS^T Q         (A from shared memory)               -> TMEM
+//   dK  += dS^T Q         (A from TMEM)                        -> TMEM
 //   dQ^T = K^T dS^T       (M = d, N 64 rows, K 128 keys)       -> TMEM
 //          read out, scaled, staged in shared memory and added into the fp32
 //          dq accumulator with one TMA reduce-add per step.
@@ -34,9 +34,11 @@
 //              S^T(s), dP^T(s), dQ^T(s-1), then dV(s) and dK(s) once P/dS(s)
 //              is ready, so dQ^T(s-1) overlaps the P/dS work of step s.
 // TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
-// P^T [384,416) | dQ^T [416,480). dS^T in shared memory is double buffered.
-// Because P^T and dS^T do not alias S^T and dP^T, the only per-step
-// handshake the MMA thread waits for is P/dS; tcgen05 commit order covers
+// P^T [384,416) | dQ^T [416,480) | dS^T [480,512). dS^T in shared memory is
+// double buffered. Because P^T and dS^T do not alias S^T and dP^T, the only
+// per-step handshake on the MMA thread's critical path is P/dS (arrived
+// right after the TMEM stores); the shared-memory copy of dS^T has its own
+// barrier, needed only by dQ^T one step later; tcgen05 commit order covers
 // the rest (an MMA's commit also covers every MMA issued before it).
 // Every mbarrier wait is bounded (2 s).
 #include <cuda.h>
@@ -55,7 +57,7 @@ constexpr int kThreads = 448;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TP = 384, TDQ = 416;
+constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TP = 384, TDQ = 416, TDS = 480;
 constexpr int kStages = 3;
 
 // dynamic shared memory (1024-aligned offsets)
@@ -73,7 +75,7 @@ constexpr int SM_STG = SM_S + 2 * kST;     // + buffer * kStg
 constexpr int kSmemBytes = SM_STG + 2 * kStg + 1024;
 
 enum : int {
-    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_DV = 10, B_DK = 11, B_DQ = 12, B_DQF = 14,
+    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_SS = 10 /* x2, by step parity */, B_DQ = 12, B_DQF = 14,
     B_COUNT = 16
 };
 
@@ -216,8 +218,12 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
 __device__ __forceinline__ void issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
                                          volatile int* abort, bool* ok) {
     constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
-    // dQ^T of the previous step must have been read out of TMEM
+    // dQ^T of the previous step must have been read out of TMEM, and this
+    // step's dS^T must be in shared memory
     if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) { *ok = false; return; }
+    // (one barrier per step parity: the P/dS warps can finish the next step
+    // before this wait, but not the one after, which needs an S^T issued later)
+    if (!mma_wait(bar, B_SS + (ts & 1), (ts >> 1) & 1, abort)) { *ok = false; return; }
     const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + (ts & 1) * kST;
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k)
@@ -258,16 +264,15 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
             if (!ok) return;
         }
         if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
-        // dV += P^T dO (P^T in TMEM); dK += dS^T Q (dS^T in shared memory, K-major)
+        // dV += P^T dO, dK += dS^T Q (P^T and dS^T in TMEM)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
             tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
                        (s > 0 || k > 0) ? 1u : 0u);
-        const uint32_t sS = sbase + SM_S + (ts & 1) * kST;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ss(tmem + TDK, tc::sdesc_sw128(sS + 32 * k, 16, 1024), tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024),
-                       id_kv, (s > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(tmem + TDK, tmem + TDS + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
+                       (s > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
     }
     if (c.n_steps > 0) issue_dq(sbase, bar, tmem, ts_base + c.n_steps - 1, c.n_steps - 1, abort, &ok);
@@ -342,6 +347,10 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
             }
         }
         tc::tmem_st16(tmem + lb + TP + 16 * g, pp);
+        tc::tmem_st16(tmem + lb + TDS + 16 * g, dd);
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_SM]));  // dV and dK may go
         {   // dS^T row kk, columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
             uint8_t* srow = smem + SM_S + (ts & 1) * kST + kk * 128;
 #pragma unroll
@@ -350,10 +359,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
                 *reinterpret_cast<uint4*>(srow + chunk * 16) = make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
             }
         }
-        tc::tmem_st_wait();
-        tc::tc_fence_before();
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_SM]));
+        tc::mbar_arrive(tc::smem_addr(&bar[B_SS + (ts & 1)]));  // dQ^T may go (issued one step later)
     }
 }
 
@@ -450,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_DP]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_SM]), 256);
-        tc::mbar_init(tc::smem_addr(&bar[B_DV]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_DK]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_SS]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_SS + 1]), 256);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tc::smem_addr(&bar[B_DQ + b]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_DQF + b]), 1);

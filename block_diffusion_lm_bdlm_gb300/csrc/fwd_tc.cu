@@ -55,7 +55,7 @@ struct Lay {
 };
 
 // barrier slots
-enum : int { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_S = 7, B_P = 9, B_O = 11, B_COUNT = 13 };
+enum : int { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_S = 7, B_P = 9, B_O = 11, B_PH = 13, B_COUNT = 15 };
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -150,12 +150,19 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
             if (i >= nh) break;
             const uint32_t ti = i == 0 ? t : t_base1 + j;
             const uint32_t tS = tmem + 128 * i, tO = tmem + 256 + D * i;
+            // P arrives in two halves (keys 0-63, then 64-127) so that the
+            // first half's PV overlaps the softmax of the second half
+            if (!tc::mbar_wait(tc::smem_addr(&bar[B_PH + i]), ti & 1, abort, kTimeoutNs)) return;
+            tc::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < BN / 32; ++k)
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o,
+                           (j > 0 || k > 0) ? 1u : 0u);
             if (!tc::mbar_wait(tc::smem_addr(&bar[B_P + i]), ti & 1, abort, kTimeoutNs)) return;
             tc::tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o,
-                           (j > 0 || k > 0) ? 1u : 0u);
+            for (int k = BN / 32; k < BN / 16; ++k)
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o, 1u);
             tc::mma_commit(tc::smem_addr(&bar[B_O + i]));
         }
         tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));
@@ -240,6 +247,9 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
             pa[e] = pack2(p0, p1);
         }
         tc::tmem_st32(tS, pa);
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_PH + i]));
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             const float p0 = ex2f(fmaf(x[64 + 2 * e], sl2, -m_eff));
@@ -332,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(tc::smem_addr(&bar[B_KVEMPTY + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_S + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_P + s]), 128);
+            tc::mbar_init(tc::smem_addr(&bar[B_PH + s]), 128);
             tc::mbar_init(tc::smem_addr(&bar[B_O + s]), 1);
         }
         tc::fence_barrier_init();

@@ -65,6 +65,12 @@ def sampled_keys_check(x, w, dk, dv, g, n, key_blocks):
         check_grad(host(dv[keys][:, g:g + 1]), r["dv"][keys], f"dv {kind} block {b}")
 
 
+def workspaces(bd, w, L, n_docs=1):
+    f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, w.heads, w.head_dim, n_docs), dtype=torch.uint8, device="cuda")
+    b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, w.heads, w.head_dim, n_docs), dtype=torch.uint8, device="cuda")
+    return f, b
+
+
 def identities_check(x, w, dk, dv):
     G = w.heads // w.kv_heads
     dk64 = dk.double()
@@ -82,16 +88,19 @@ def test_long128k_sharded_forward_merge_backward(bd):
     x = synth.make_inputs(w, device="cuda")
     n, B = w.n, w.block
     windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+    wsf, wsb = workspaces(bd, w, 2 * n)
     parts, lses = [], []
     for lo, hi in windows:
-        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], B, part=bd.Partial.window(lo, hi))
+        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], B, part=bd.Partial.window(lo, hi), workspace=wsf)
+        assert bd.bdlm_read_error(wsf) == 0
         parts.append(po)
         lses.append(pl)
     o, lse = bd.bdlm_lse_merge(parts, lses)
     del parts
-    uo, ul = bd.bdlm_attn_fwd(x.q, x.k, x.v, B)
-    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B)
-    torch.cuda.synchronize()
+    uo, ul = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, workspace=wsf)
+    assert bd.bdlm_read_error(wsf) == 0
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, workspace=wsb)
+    assert bd.bdlm_read_error(wsb) == 0
     # sharded + merged == unsharded (both on the GPU)
     assert (o.float() - uo.float()).abs().max().item() <= 2e-2
     assert ((lse - ul).abs() / ul.abs().clamp(min=1.0)).max().item() <= 1e-3
@@ -109,7 +118,9 @@ def test_vlong256k_block_groups_and_backward(bd):
     x = synth.make_inputs(w, device="cuda")
     n, B = w.n, w.block
     nb = n // B
-    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B)
+    wsf, wsb = workspaces(bd, w, 2 * n)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, workspace=wsf)
+    assert bd.bdlm_read_error(wsf) == 0
     groups = synth.early_late_groups(nb, w.groups)
     worst_o, worst_l = 0.0, 0.0
     clean_pos = torch.arange(n, device="cuda")
@@ -118,13 +129,13 @@ def test_vlong256k_block_groups_and_backward(bd):
         corr = (n + bl.long()[:, None] * B + torch.arange(B, device="cuda")[None]).reshape(-1)
         kpos = torch.cat([clean_pos, corr])
         go, gl = bd.bdlm_attn_fwd(x.q[corr].contiguous(), x.k[kpos].contiguous(), x.v[kpos].contiguous(), B,
-                                  L=2 * n, part=bd.Partial.group(bl))
-        torch.cuda.synchronize()
+                                  L=2 * n, part=bd.Partial.group(bl), workspace=wsf)
+        assert bd.bdlm_read_error(wsf) == 0
         worst_o = max(worst_o, (go.float() - o[corr].float()).abs().max().item())
         worst_l = max(worst_l, ((gl - lse[:, corr]).abs() / lse[:, corr].abs().clamp(min=1.0)).max().item())
     assert worst_o <= 2e-2 and worst_l <= 1e-3, (worst_o, worst_l)
-    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B)
-    torch.cuda.synchronize()
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, workspace=wsb)
+    assert bd.bdlm_read_error(wsb) == 0
     # the early/late pair of group 0 and a middle block, clean and corrupted
     blocks = [(0, 0), (0, (nb - 1) * B), (0, n), (0, n + (nb - 1) * B), (0, n + (nb // 2) * B)]
     sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 3], blocks=blocks)
@@ -138,9 +149,11 @@ def test_packed_documents_full_size(bd):
     cu = x.cu_seqlens
     cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
     B = w.block
-    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, cu_seqlens=cu_d)
-    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, cu_seqlens=cu_d)
-    torch.cuda.synchronize()
+    wsf, wsb = workspaces(bd, w, cu[-1], len(cu) - 1)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, cu_seqlens=cu_d, workspace=wsf)
+    assert bd.bdlm_read_error(wsf) == 0
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, cu_seqlens=cu_d, workspace=wsb)
+    assert bd.bdlm_read_error(wsb) == 0
     lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
     # two short documents in full (all gradients, one kv group)
     short = sorted(range(len(lens)), key=lambda i: lens[i])[:2]
