@@ -80,10 +80,10 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, tag="timed"):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{tag}_gpu{index}.csv")
 
     def start(self):
         try:
@@ -105,7 +105,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, pw = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
@@ -114,12 +114,14 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx = float(parts[2])
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "sm_mhz_min": min(sm) if sm else None, "power_w_median": statistics.median(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -366,19 +368,22 @@ def end_to_end(step, x, flops, args, world, dev):
 
     one_step()  # untimed: the first use of freshly pinned host buffers is slow
     torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index, tag="e2e")
+    sampler.start()
     barrier(world, dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    evs[0].record()
+    for i in range(e2e_steps):
         one_step()
-    e1.record()
+        evs[i + 1].record()
     torch.cuda.synchronize()
     barrier(world, dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    clocks = sampler.stop()
+    e2e_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), world, dev)
     e2e_value = flops * world * e2e_steps / (e2e_ms / 1e3) / 1e12
     return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps}
+            "steps": e2e_steps, "ms_per_step": [evs[i].elapsed_time(evs[i + 1]) for i in range(e2e_steps)],
+            "clocks": clocks}
 
 
 def l2_note(x):
