@@ -208,14 +208,19 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
     return out, lse
 
 
-def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, cu_seqlens=None, softmax_scale: float = 0.0,
-                  dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """BDLM attention backward of the full forward. Returns (dq, dk, dv) bf16."""
+def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, L: Optional[int] = None, cu_seqlens=None,
+                  softmax_scale: float = 0.0, part: Optional[Partial] = None, dq=None, dk=None, dv=None,
+                  workspace=None, stream=None):
+    """BDLM attention backward. q/o/dO [Lq,H,d], k/v [Lk,Hk,d] bf16 CUDA
+    tensors, lse [H,Lq] fp32. L defaults to q's rows and must be given as 2n
+    for a block group. With Partial.window, o and lse are the merged full
+    forward's and dq is the window's share. Returns (dq, dk, dv) bf16."""
     lib = load_library()
     for nm, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
         _bf16_cuda(nm, t)
-    L, H, d = q.shape
+    Lq, H, d = q.shape
     Hk = k.shape[1]
+    L = Lq if L is None else int(L)
     cu_ptr, n_docs = _cu(cu_seqlens)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -223,9 +228,10 @@ def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, cu_seqlens=None, softmax_s
     ws_bytes = lib.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    cpart = ctypes.byref(part.c()) if part is not None else None
     st = lib.bdlm_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), L, block, H, Hk, d, cu_ptr, n_docs,
-                           softmax_scale, None, workspace.data_ptr(), workspace.numel(), _stream(stream))
+                           softmax_scale, cpart, workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check(st, "bdlm_attn_bwd")
     return dq, dk, dv
 

@@ -205,10 +205,9 @@ int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
                   int32_t head_dim, const int32_t* cu_seqlens, int32_t n_docs, float softmax_scale,
                   const bdlm_partial* part, void* workspace, size_t workspace_bytes, bdlm_stream_t stream) {
     g_launches = 0;
-    if (part && part->kind != BDLM_PART_NONE) return BDLM_ERR_UNSUPPORTED;
     Layout lay;
     Common cm{};
-    int st = check_common(q, k, v, L, block, heads, kv_heads, head_dim, cu_seqlens, n_docs, nullptr, &lay, &cm);
+    int st = check_common(q, k, v, L, block, heads, kv_heads, head_dim, cu_seqlens, n_docs, part, &lay, &cm);
     if (st != BDLM_OK) return st;
     if (!o || !lse || !dO || !dq || !dk || !dv) return BDLM_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
@@ -245,7 +244,8 @@ int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
     a.D = head_dim;
     a.scale = pick_scale(softmax_scale, head_dim);
     a.scale_log2 = a.scale * 1.4426950408889634f;
-    a.L = L;
+    a.Lq = cm.Lq;
+    a.Lk = cm.Lk;
     a.table = ws.table;
     a.hdr = ws.hdr;
     if (launch_bwd(a, sms, s, &launches) != cudaSuccess) return BDLM_ERR_CUDA;

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     constexpr int LPR = D / 8;  // lanes per (row, head)
     const long long pair = ((long long)blockIdx.x * 256 + threadIdx.x) / LPR;
     const int c = threadIdx.x % LPR;
-    const long long n_pairs = a.L * a.H;
+    const long long n_pairs = a.Lq * a.H;
     const bool ok = pair < n_pairs;  // whole lane groups are in or out
     const long long row = ok ? pair / a.H : 0;
     const int h = ok ? (int)(pair % a.H) : 0;
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, LPR);
     if (!ok) return;
-    if (c == 0) a.Dsum[(long long)h * a.L + row] = s;
+    if (c == 0) a.Dsum[(long long)h * a.Lq + row] = s;
     float4* acc = reinterpret_cast<float4*>(a.dqacc + off);
     acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 template <int D>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdArgs a) {
     const long long i = (long long)blockIdx.x * 256 + threadIdx.x;  // 8 elements each
-    const long long n = a.L * a.H * D / 8;
+    const long long n = a.Lq * a.H * D / 8;
     if (i >= n) return;
     const float4 x = reinterpret_cast<const float4*>(a.dqacc)[2 * i];
     const float4 y = reinterpret_cast<const float4*>(a.dqacc)[2 * i + 1];
@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
     const long long q_stride = (long long)H * D;
     const long long k_stride = (long long)a.Hk * D;
     const float sl2 = a.scale_log2;
-    const int B = a.lay.B;
 
     for (;;) {
         if (tid == 0) s_item = atomicAdd(&a.hdr->counter, 1);
@@ -112,24 +111,14 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
         const Tile kt = a.table[item / a.Hk];
         const int kvh = item % a.Hk;
         const int n = kt.n;
-        const int k0 = kt.doc_start + kt.pos0;  // first k row of the item
+        const int k0 = key_row0(a.lay, kt);  // first k row of the item
         const int kv_rows = kt.nrows;
 
-        // query ranges (document positions) that see these keys
-        int ra_lo, ra_hi, rb_lo = 0, rb_hi = 0;
-        if (kt.pos0 < n) {
-            const int b = kt.pos0 / B;
-            ra_lo = b * B;
-            ra_hi = n;
-            rb_lo = n + (b + 1) * B;
-            rb_hi = 2 * n;
-        } else {
-            const int b0 = (kt.pos0 - n) / B, b1 = (kt.pos0 + kv_rows - 1 - n) / B;
-            ra_lo = n + b0 * B;
-            ra_hi = n + (b1 + 1) * B;
-        }
+        // query ranges (row positions) that see these keys
+        const KeyRows kr = key_tile_rows(a.lay, kt);
+        const int ra_lo = kr.a_lo, ra_hi = kr.a_hi, rb_lo = kr.b_lo, rb_hi = kr.b_hi;
         const int na = (ra_hi - ra_lo + BQ - 1) / BQ;
-        const int nb = rb_hi > rb_lo ? (rb_hi - rb_lo + BQ - 1) / BQ : 0;
+        const int nb = (rb_hi - rb_lo + BQ - 1) / BQ;
         const int per_head = na + nb;
         const int n_steps = per_head * G;
 
@@ -152,9 +141,9 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
                 s_span[buf][tid] = sp;
                 float l2 = INFINITY, dd = 0.f;
                 if (tid < qt.nrows) {
-                    const float lse = a.lse[(long long)h * a.L + qr0 + tid];
+                    const float lse = a.lse[(long long)h * a.Lq + qr0 + tid];
                     l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
-                    dd = a.Dsum[(long long)h * a.L + qr0 + tid];
+                    dd = a.Dsum[(long long)h * a.Lq + qr0 + tid];
                 }
                 s_lse2[buf][tid] = l2;
                 s_D[buf][tid] = dd;
@@ -308,7 +297,7 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
 
 template <int D>
 cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
-    const long long pairs = a.L * a.H;
+    const long long pairs = a.Lq * a.H;
     const long long pre_threads = pairs * (D / 8);
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();

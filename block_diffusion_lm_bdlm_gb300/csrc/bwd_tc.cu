@@ -129,23 +129,15 @@ __device__ __forceinline__ ItemCtx decode(const BwdArgs& a, int item) {
     ItemCtx c;
     c.kt = a.table[item / a.Hk];
     c.kvh = item % a.Hk;
-    const int n = c.kt.n, B = a.lay.B;
-    c.k0 = c.kt.doc_start + c.kt.pos0;
+    c.k0 = key_row0(a.lay, c.kt);
     c.kv_rows = c.kt.nrows;
-    c.rb_lo = c.rb_hi = 0;
-    if (c.kt.pos0 < n) {
-        const int b = c.kt.pos0 / B;
-        c.ra_lo = b * B;
-        c.ra_hi = n;
-        c.rb_lo = n + (b + 1) * B;
-        c.rb_hi = 2 * n;
-    } else {
-        const int b0 = (c.kt.pos0 - n) / B, b1 = (c.kt.pos0 + c.kv_rows - 1 - n) / B;
-        c.ra_lo = n + b0 * B;
-        c.ra_hi = n + (b1 + 1) * B;
-    }
+    const KeyRows r = key_tile_rows(a.lay, c.kt);
+    c.ra_lo = r.a_lo;
+    c.ra_hi = r.a_hi;
+    c.rb_lo = r.b_lo;
+    c.rb_hi = r.b_hi;
     c.na = (c.ra_hi - c.ra_lo + BQ - 1) / BQ;
-    const int nb = c.rb_hi > c.rb_lo ? (c.rb_hi - c.rb_lo + BQ - 1) / BQ : 0;
+    const int nb = (c.rb_hi - c.rb_lo + BQ - 1) / BQ;
     c.per_head = c.na + nb;
     c.n_steps = c.per_head * a.G;
     return c;
@@ -197,7 +189,7 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
             const int r = 2 * lane + u;
             float nl2 = 0.f, dd = 0.f;
             if (r < nrows) {
-                const long long gi = (long long)h * a.L + qr0 + r;
+                const long long gi = (long long)h * a.Lq + qr0 + r;
                 nl2 = -__ldg(a.lse + gi) * 1.4426950408889634f;
                 dd = __ldg(a.Dsum + gi);
             }
@@ -287,31 +279,19 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
     const int kk = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale_log2;
-    // Rows (document positions) that see this thread's key, per half: a clean
-    // key of block b is seen by clean rows of blocks >= b and corrupted rows of
-    // blocks > b; a corrupted key only by the corrupted rows of its block.
-    const int n = c.kt.n, B = a.lay.B, kc = c.kt.pos0 + kk;
-    int A0 = 0, A1 = 0, C0 = 0, C1 = 0;
-    if (kk < c.kv_rows) {
-        if (kc < n) {
-            const int bk = kc / B;
-            A0 = bk * B;
-            A1 = n;
-            C0 = n + (bk + 1) * B;
-            C1 = 2 * n;
-        } else {
-            C0 = n + ((kc - n) / B) * B;
-            C1 = C0 + B;
-        }
-    }
+    // Row positions that see this thread's key, one interval per query range:
+    // a clean key of block b is seen by clean rows of blocks >= b and corrupted
+    // rows of blocks > b; a corrupted key only by the corrupted rows of its block.
+    const KeyRows kr = key_rows(a.lay, c.kt, kk);
     int rem = 0;  // step index within the current query head
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
-        const int p0 = rem < c.na ? c.ra_lo + rem * BQ : c.rb_lo + (rem - c.na) * BQ;
-        const int nrows = imin(BQ, (rem < c.na ? c.ra_hi : c.rb_hi) - p0);
+        const bool in_a = rem < c.na;
+        const int p0 = in_a ? c.ra_lo + rem * BQ : c.rb_lo + (rem - c.na) * BQ;
+        const int nrows = imin(BQ, (in_a ? c.ra_hi : c.rb_hi) - p0);
         if (++rem == c.per_head) rem = 0;
-        const int lo = imax((p0 < n ? A0 : C0) - p0, 0) - 32 * g;  // relative to this group's first column
-        const int hi = imin((p0 < n ? A1 : C1) - p0, nrows) - 32 * g;
+        const int lo = imax((in_a ? kr.a_lo : kr.b_lo) - p0, 0) - 32 * g;  // relative to this group's first column
+        const int hi = imin((in_a ? kr.a_hi : kr.b_hi) - p0, nrows) - 32 * g;
         const int len = imax(hi - lo, 0);
         const bool all_visible = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
         bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts / kStages) & 1, abort, kTimeoutNs);
@@ -404,9 +384,12 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
             }
         }
     }
-    // dK and dV: the last dQ^T commit covered every MMA of the item
+    // dK and dV: the last dQ^T commit covered every MMA of the item. Keys that
+    // no query row of the call sees (clean keys after a block group's last
+    // block) get zeros; their TMEM columns were never written for this item.
     const int kk = dl;
     const bool key_ok = kk < c.kv_rows;
+    const bool seen = c.n_steps > 0;
     const long long rowoff = (long long)(c.k0 + kk) * ((long long)a.Hk * D) + (long long)c.kvh * D;
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
@@ -416,8 +399,13 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
             uint32_t v[32];
-            tc::tmem_ld32(tmem + lb + src + 32 * q, v);
-            tc::tmem_ld_wait();
+            if (seen) {
+                tc::tmem_ld32(tmem + lb + src + 32 * q, v);
+                tc::tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
             if (key_ok) {
                 uint4* o = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
@@ -550,11 +538,11 @@ bool make_map(CUtensorMap* m, const void* base, bool f32, int heads, long long r
 
 cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st) {
     CUtensorMap mk, mv, mq, mdo, mdq;
-    if (!make_map(&mk, a.k, false, a.Hk, a.L, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, a.v, false, a.Hk, a.L, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mq, a.q, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdo, a.dO, false, a.H, a.L, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdq, a.dqacc, true, a.H, a.L, D, kHalfRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_map(&mk, a.k, false, a.Hk, a.Lk, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, a.v, false, a.Hk, a.Lk, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mq, a.q, false, a.H, a.Lq, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mdo, a.dO, false, a.H, a.Lq, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mdq, a.dqacc, true, a.H, a.Lq, D, kHalfRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;

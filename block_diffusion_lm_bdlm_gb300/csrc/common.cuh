@@ -155,6 +155,94 @@ __device__ __forceinline__ RelInterval range_interval(const Span& s, bool prefix
 }
 __device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) { return (unsigned)(e - r.lo) < r.len; }
 
+// ---------------------------------------------------------------------------
+// Key-major view (backward). A backward tile is a run of consecutive keys that
+// never straddles the clean/corrupted boundary. Tile.pos0 is the sequence
+// position of key 0 (full: document position; window: global position) or,
+// for a block group, its k row (clean keys [0, n), then the group's corrupted
+// rows). "Row positions" of the query side map to q rows as doc_start + p
+// (full), p (window: q holds the whole sequence) or the list row p (group).
+// ---------------------------------------------------------------------------
+
+// Number of list entries with block id <= b. The backward requires a strictly
+// ascending block list, so the group rows that see a clean key of block b are
+// the list rows from group_count_le(b) * B on.
+__device__ __forceinline__ int group_count_le(const Layout& lay, int b) {
+    int lo = 0, hi = lay.n_blocks;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(lay.blocks + mid) <= b) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+// k row of key 0 of backward tile t.
+__device__ __forceinline__ int key_row0(const Layout& lay, const Tile& t) {
+    return lay.mode == MODE_WINDOW ? t.pos0 - lay.kw_lo : t.doc_start + t.pos0;
+}
+
+// The query rows that see key tile t: at most two row-position ranges (range
+// a, then range b; empty ranges are [0, 0)). For a clean key of block b the
+// rows are the clean rows of blocks >= b and the corrupted rows of blocks > b;
+// for a corrupted key, the corrupted rows of its own block.
+struct KeyRows {
+    int a_lo, a_hi, b_lo, b_hi;
+};
+__device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& t) {
+    KeyRows r{0, 0, 0, 0};
+    const int n = t.n, B = lay.B;
+    if (lay.mode == MODE_GROUP) {
+        const int R = lay.n_blocks * B;
+        if (t.pos0 < n) {
+            const int lo = group_count_le(lay, t.pos0 / B) * B;
+            if (lo < R) { r.a_lo = lo; r.a_hi = R; }
+        } else {
+            r.a_lo = ((t.pos0 - n) / B) * B;
+            r.a_hi = ((t.pos0 + t.nrows - 1 - n) / B + 1) * B;
+        }
+        return r;
+    }
+    if (t.pos0 < n) {
+        const int b = t.pos0 / B;
+        r.a_lo = b * B;
+        r.a_hi = n;
+        if ((b + 1) * B < n) { r.b_lo = n + (b + 1) * B; r.b_hi = 2 * n; }
+    } else {
+        r.a_lo = n + ((t.pos0 - n) / B) * B;
+        r.a_hi = n + ((t.pos0 + t.nrows - 1 - n) / B + 1) * B;
+    }
+    return r;
+}
+
+// The same for key kk of tile t alone (one interval per range; all empty for
+// kk >= t.nrows).
+__device__ __forceinline__ KeyRows key_rows(const Layout& lay, const Tile& t, int kk) {
+    KeyRows r{0, 0, 0, 0};
+    if (kk >= t.nrows) return r;
+    const int n = t.n, B = lay.B, kc = t.pos0 + kk;
+    if (lay.mode == MODE_GROUP) {
+        if (kc < n) {
+            r.a_lo = group_count_le(lay, kc / B) * B;
+            r.a_hi = lay.n_blocks * B;
+        } else {
+            r.a_lo = ((kc - n) / B) * B;
+            r.a_hi = r.a_lo + B;
+        }
+        return r;
+    }
+    if (kc < n) {
+        const int bk = kc / B;
+        r.a_lo = bk * B;
+        r.a_hi = n;
+        r.b_lo = n + (bk + 1) * B;
+        r.b_hi = 2 * n;
+    } else {
+        r.a_lo = n + ((kc - n) / B) * B;
+        r.a_hi = r.a_lo + B;
+    }
+    return r;
+}
+
 __device__ __forceinline__ void set_error(WsHeader* h, int code, int info) {
     if (atomicCAS(&h->error, 0, code) == 0) atomicExch(&h->info, info);
 }

@@ -47,7 +47,7 @@ struct BwdArgs {
     Layout lay;
     int H, Hk, G, D;
     float scale, scale_log2;
-    long long L;
+    long long Lq, Lk;  // rows of q (o, dO, dq, lse, D) and of k (v, dk, dv)
     const Tile* table;
     WsHeader* hdr;
 };

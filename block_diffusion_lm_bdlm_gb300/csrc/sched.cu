@@ -68,13 +68,8 @@ __device__ int fwd_cost(const TileRange& g, int kn) {
 
 // Cost of a backward key tile, in query rows that see it.
 __device__ int bwd_cost(const Layout& lay, const Tile& t) {
-    const int n = t.n, B = lay.B;
-    if (t.pos0 < n) {
-        int b = t.pos0 / B;
-        return (n - b * B) + imax(0, n - (b + 1) * B);
-    }
-    int b0 = (t.pos0 - n) / B, b1 = (t.pos0 + t.nrows - 1 - n) / B;
-    return (b1 - b0 + 1) * B;
+    const KeyRows r = key_tile_rows(lay, t);
+    return (r.a_hi - r.a_lo) + (r.b_hi - r.b_lo);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -115,6 +110,8 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         for (int i = tid; i < lay.n_blocks; i += kThreads) {
             int b = __ldg(lay.blocks + i);
             if (b < 0 || b >= nb) { bad = 1; bad_info = i; }
+            // the key-major backward needs the list strictly ascending
+            if (kind == 1 && i > 0 && b <= __ldg(lay.blocks + i - 1)) { bad = 1; bad_info = i; }
         }
     }
     if (__syncthreads_or(bad)) {
@@ -123,7 +120,32 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     }
 
     // ---- enumeration ---------------------------------------------------------
-    if (lay.mode == MODE_GROUP) {
+    if (kind == 1 && lay.mode != MODE_FULL) {
+        // key tiles over the call's keys, in two runs that never straddle the
+        // clean/corrupted boundary: sequence positions of the window, or the
+        // group's k rows (clean [0, n), then its corrupted rows)
+        int c_lo, c_hi, x_lo, x_hi;
+        if (lay.mode == MODE_WINDOW) {
+            c_lo = lay.kw_lo;
+            c_hi = imin(lay.kw_hi, lay.n);
+            x_lo = imax(lay.kw_lo, lay.n);
+            x_hi = lay.kw_hi;
+        } else {
+            c_lo = 0;
+            c_hi = lay.n;
+            x_lo = lay.n;
+            x_hi = lay.n + lay.n_blocks * lay.B;
+        }
+        const int nc = c_hi > c_lo ? (c_hi - c_lo + tile_rows - 1) / tile_rows : 0;
+        const int nx = x_hi > x_lo ? (x_hi - x_lo + tile_rows - 1) / tile_rows : 0;
+        for (int i = tid; i < nc + nx && i < max_tiles; i += kThreads) {
+            const bool cl = i < nc;
+            const int p0 = cl ? c_lo + i * tile_rows : x_lo + (i - nc) * tile_rows;
+            tmp[i] = Tile{0, lay.n, p0, imin(tile_rows, (cl ? c_hi : x_hi) - p0)};
+        }
+        if (tid == 0) s_carry = nc + nx;
+        __syncthreads();
+    } else if (lay.mode == MODE_GROUP) {
         const int rows = lay.n_blocks * lay.B;
         const int nt = (rows + tile_rows - 1) / tile_rows;
         for (int i = tid; i < nt && i < max_tiles; i += kThreads)

@@ -148,12 +148,33 @@ BDLM_API int bdlm_attn_fwd_noalloc(const void* q, const void* k, const void* v, 
                   const bdlm_partial* part, bdlm_stream_t stream);
 
 /*
- * Backward of the full forward (part must be NULL or kind NONE): given q, k, v,
- * the forward's o and lse, and the upstream gradient dO, writes
- * dq [L, H, d], dk [L, Hk, d], dv [L, Hk, d] (bf16). dk and dv sum the
+ * Backward: given q, k, v, the forward's o and lse, and the upstream gradient
+ * dO, writes dq [Lq, H, d], dk [Lk, Hk, d], dv [Lk, Hk, d] (bf16), the
+ * gradients of softmax(QK^T)V under the BDLM mask ("Efficient Long-context
+ * Language Model Training by Core Attention Disaggregation", abstract, for
+ * core attention; the mask as for bdlm_attn_fwd). dk and dv sum the
  * contributions of all H/Hk query heads that share a kv head. The workspace
- * (>= bdlm_attn_bwd_workspace_bytes) holds D = rowsum(dO * o) and an fp32 dq
- * accumulator; its contents need no initialisation.
+ * (>= bdlm_attn_bwd_workspace_bytes(L, ...)) holds D = rowsum(dO * o) and an
+ * fp32 dq accumulator; its contents need no initialisation.
+ *
+ *   part NULL / NONE  the full attention; Lq = Lk = L.
+ *   KEY_WINDOW        one clean-K/V shard (or the local corrupted keys) under
+ *                     context-sharded block parallelism (Block Parallelism
+ *                     abstract; rit.work CSBP post, CSBP paragraph): k, v hold
+ *                     the keys at positions [key_lo, key_hi); q, dO hold all L
+ *                     rows; o and lse are the MERGED (full) forward results,
+ *                     not the shard's partial ones. Writes this window's share
+ *                     of dq (summed over a partition of the keys, the shares
+ *                     give the full dq) and the window keys' complete dk, dv.
+ *   BLOCK_GROUP       one rank's corrupted target blocks (same layout as the
+ *                     forward; o, lse from the group's forward). dq is complete
+ *                     for the group's rows and dk, dv for its corrupted keys;
+ *                     for the clean keys dk, dv hold the group's share only
+ *                     (the shares of all groups plus the clean rows' own sum
+ *                     to the full gradient). The block list must be strictly
+ *                     ascending here (BDLM_ERR_DEVICE_CHECK otherwise, with
+ *                     the offending list index). Clean keys that no listed
+ *                     block sees get zero gradients.
  */
 BDLM_API int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dO, void* dq, void* dk, void* dv,

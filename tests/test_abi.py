@@ -103,10 +103,16 @@ def test_forward_rejects_bad_arguments(lib):
 def test_backward_and_merge_reject_bad_arguments(lib):
     import block_diffusion_lm_bdlm_gb300 as bd
 
-    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None)
-    st = lib.bdlm_attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, 16, 2, 2, 64, None, 1, 0.0,
-                           ctypes.byref(p), 256, 1 << 20, None)
-    assert st == 2
+    def bwd(part, cu=None):
+        return lib.bdlm_attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, 16, 2, 2, 64, cu, 1, 0.0,
+                                 ctypes.byref(part), 256, 1 << 20, None)
+
+    # partial backward: the same descriptor checks as the forward
+    assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None), cu=256) == 2  # windows need one sequence
+    assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 10, 5, None)) == 1         # hi <= lo
+    assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 257, None)) == 1        # past the sequence
+    assert bwd(bd._CPartial(bd.PART_BLOCK_GROUP, 0, 0, 0, None)) == 1         # no block list
+    assert bwd(bd._CPartial(bd.PART_BLOCK_GROUP, 9, 0, 0, 16)) == 1           # more blocks than n / B
     st = lib.bdlm_attn_bwd(16, 16, 16, 16, 16, None, 16, 16, 16, 256, 16, 2, 2, 64, None, 1, 0.0, None, 256,
                            1 << 20, None)
     assert st == 1

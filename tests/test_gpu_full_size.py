@@ -111,6 +111,20 @@ def test_long128k_sharded_forward_merge_backward(bd):
     sampled_keys_check(x, w, dk, dv, g=3, n=n, key_blocks=[("clean", nb - 1), ("clean", nb - 2), ("corrupted", 0),
                                                            ("corrupted", nb // 2)])
     identities_check(x, w, dk, dv)
+    # sharded backward: per-shard calls with the merged o and lse; the dq
+    # shares sum to the unsharded dq and the shards' dk, dv tile it
+    dq_sum = torch.zeros(dq.shape, dtype=torch.float32, device="cuda")
+    for lo, hi in windows:
+        sq, sk, sv = bd.bdlm_attn_bwd(x.q, x.k[lo:hi], x.v[lo:hi], o, lse, x.do, B,
+                                      part=bd.Partial.window(lo, hi), workspace=wsb)
+        assert bd.bdlm_read_error(wsb) == 0
+        dq_sum += sq.float()
+        del sq
+        for got, ref, nm in ((sk, dk[lo:hi], "dk"), (sv, dv[lo:hi], "dv")):
+            rel = ((got.float() - ref.float()).norm() / ref.float().norm()).item()
+            assert rel <= 1e-2, f"{nm} of shard [{lo},{hi}): {rel:.3e}"
+    rel = ((dq_sum - dq.float()).norm() / dq.float().norm()).item()
+    assert rel <= 1e-2, f"sum of dq shares: {rel:.3e}"
 
 
 def test_vlong256k_block_groups_and_backward(bd):
@@ -141,6 +155,32 @@ def test_vlong256k_block_groups_and_backward(bd):
     sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 3], blocks=blocks)
     sampled_keys_check(x, w, dk, dv, g=1, n=n, key_blocks=[("clean", nb - 1), ("corrupted", 5)])
     identities_check(x, w, dk, dv)
+    # block-group backward of every group: dq of the group's rows and dk, dv
+    # of its corrupted keys equal the unsplit backward's; for group 0, the
+    # group's share of dk, dv of a late clean key block against the oracle
+    G = w.heads // w.kv_heads
+    for gi, blocks in enumerate(groups):
+        bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
+        corr = (n + bl.long()[:, None] * B + torch.arange(B, device="cuda")[None]).reshape(-1)
+        kpos = torch.cat([clean_pos, corr])
+        part = bd.Partial.group(bl)
+        qg, kg, vg, dog = x.q[corr].contiguous(), x.k[kpos].contiguous(), x.v[kpos].contiguous(), x.do[corr].contiguous()
+        go, gl = bd.bdlm_attn_fwd(qg, kg, vg, B, L=2 * n, part=part, workspace=wsf)
+        gq, gk, gv = bd.bdlm_attn_bwd(qg, kg, vg, go, gl, dog, B, L=2 * n, part=part, workspace=wsb)
+        assert bd.bdlm_read_error(wsb) == 0
+        for got, ref, nm in ((gq, dq[corr], "dq"), (gk[n:], dk[corr], "dk"), (gv[n:], dv[corr], "dv")):
+            rel = ((got.float() - ref.float()).norm() / ref.float().norm()).item()
+            assert rel <= 1e-2, f"group {gi} {nm}: {rel:.3e}"
+        if gi == 0:
+            b = nb - 64  # seen by the group's blocks after it (a few late ones)
+            seers = [(0, n + bb * B) for bb in blocks if bb > b]
+            keys = np.arange(b * B, (b + 1) * B)
+            for g in (0, w.kv_heads - 1):
+                q, k, v, do = (f32(t) for t in group_slices(x, w, g))
+                r = oracle.bdlm_attention(q, k, v, B, w.scale, do=do, row_blocks=seers)
+                check_grad(host(gk[keys][:, g:g + 1]), r["dk"][keys], f"group 0 dk clean block {b}")
+                check_grad(host(gv[keys][:, g:g + 1]), r["dv"][keys], f"group 0 dv clean block {b}")
+        del go, gl, gq, gk, gv, qg, kg, vg, dog
 
 
 def test_packed_documents_full_size(bd):

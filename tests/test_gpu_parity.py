@@ -172,6 +172,92 @@ def test_block_groups(bd, n, block, H, Hk, groups):
         assert (gl - lse[:, qi]).abs().max().item() <= 1e-3 * max(1.0, lse.abs().max().item())
 
 
+# sharded backward: each clean-K/V shard (and the local corrupted keys) with
+# the merged forward's o and lse; shares of dq sum to the full dq
+SHARDED = [
+    # n, block, H, Hk, d, shards
+    (256, 16, 2, 2, 64, 2),    # the tiny workload's shape and split (warp-level kernel)
+    (320, 32, 8, 2, 128, 3),   # uneven shards, not block-aligned
+    (96, 16, 4, 1, 128, 8),    # windows shorter than one block
+    (200, 8, 3, 3, 64, 3),     # odd heads, ragged
+]
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,shards", SHARDED)
+def test_sharded_backward(bd, n, block, H, Hk, d, shards):
+    w, x = gen(n, block, H, Hk, d, seed=3 * n + shards)
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, do=do64)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    ws = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(2 * n, H, d, 1), dtype=torch.uint8, device="cuda")
+    dq_sum = torch.zeros(2 * n, H, d, dtype=torch.float32, device="cuda")
+    dk_cat, dv_cat = torch.empty_like(x.k), torch.empty_like(x.v)
+    for lo, hi in synth.shard_bounds(n, shards) + [(n, 2 * n)]:
+        dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), o, lse, x.do, block,
+                                      part=bd.Partial.window(lo, hi), workspace=ws)
+        assert bd.bdlm_read_error(ws) == 0
+        r = oracle.partial_attention(q64, k64[lo:hi], v64[lo:hi], n, block, lo, hi, w.scale, do=do64,
+                                     o_full=full["o"], lse_full=full["lse"])
+        check_grad(host(dq), r["dq"], f"dq share [{lo},{hi})")
+        check_grad(host(dk), r["dk"], f"dk [{lo},{hi})")
+        check_grad(host(dv), r["dv"], f"dv [{lo},{hi})")
+        dq_sum += dq.float()
+        dk_cat[lo:hi] = dk
+        dv_cat[lo:hi] = dv
+    torch.cuda.synchronize()
+    check_grad(host(dq_sum), full["dq"], "sum of dq shares")
+    check_grad(host(dk_cat), full["dk"], "dk over all shards")
+    check_grad(host(dv_cat), full["dv"], "dv over all shards")
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,groups", [(512, 16, 4, 2, 128, 4), (384, 32, 2, 1, 128, 3),
+                                                   (256, 16, 2, 2, 64, 3)])
+def test_block_group_backward(bd, n, block, H, Hk, d, groups):
+    w, x = gen(n, block, H, Hk, d, seed=13 + n)
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    dq_full, dk_full, dv_full = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block)
+    ws = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(2 * n, H, d, 1), dtype=torch.uint8, device="cuda")
+    nb = n // block
+    # the early/late groups, plus a group of early blocks only: clean keys
+    # from its last block on are seen by none of its rows (zero gradient)
+    lists = synth.early_late_groups(nb, groups) + [[0, 2]]
+    for blocks in lists:
+        qpos, kpos = oracle.group_positions(n, block, blocks)
+        qi, ki = torch.from_numpy(qpos).cuda(), torch.from_numpy(kpos).cuda()
+        bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
+        part = bd.Partial.group(bl)
+        qg, kg, vg, dog = (t[i].contiguous() for t, i in ((x.q, qi), (x.k, ki), (x.v, ki), (x.do, qi)))
+        go, gl = bd.bdlm_attn_fwd(qg, kg, vg, block, L=2 * n, part=part)
+        dq, dk, dv = bd.bdlm_attn_bwd(qg, kg, vg, go, gl, dog, block, L=2 * n, part=part, workspace=ws)
+        assert bd.bdlm_read_error(ws) == 0
+        r = oracle.group_attention(q64[qpos], k64[kpos], v64[kpos], n, block, blocks, w.scale, do=do64[qpos])
+        check_grad(host(dq), r["dq"], f"group {blocks[:2]} dq")
+        check_grad(host(dk), r["dk"], f"group {blocks[:2]} dk")
+        check_grad(host(dv), r["dv"], f"group {blocks[:2]} dv")
+        # dq of the group's rows and dk, dv of its corrupted keys are complete
+        corr = slice(n, None)
+        assert (dq.float() - dq_full[qi].float()).norm() <= 1e-2 * dq_full[qi].float().norm()
+        assert (dk[corr].float() - dk_full[qi].float()).norm() <= 1e-2 * dk_full[qi].float().norm()
+        assert (dv[corr].float() - dv_full[qi].float()).norm() <= 1e-2 * dv_full[qi].float().norm()
+        unseen = max(blocks) * block
+        assert torch.all(dk[unseen:n] == 0) and torch.all(dv[unseen:n] == 0)
+
+
+def test_block_group_backward_needs_ascending_blocks(bd):
+    n, block, H, Hk, d = 128, 16, 2, 1, 128
+    w, x = gen(n, block, H, Hk, d, seed=17)
+    blocks = [5, 1]
+    qpos, kpos = oracle.group_positions(n, block, blocks)
+    qi, ki = torch.from_numpy(qpos).cuda(), torch.from_numpy(kpos).cuda()
+    part = bd.Partial.group(torch.tensor(blocks, dtype=torch.int32, device="cuda"))
+    qg, kg, vg, dog = (t[i].contiguous() for t, i in ((x.q, qi), (x.k, ki), (x.v, ki), (x.do, qi)))
+    go, gl = bd.bdlm_attn_fwd(qg, kg, vg, block, L=2 * n, part=part)  # the forward takes any order
+    ws = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(2 * n, H, d, 1), dtype=torch.uint8, device="cuda")
+    bd.bdlm_attn_bwd(qg, kg, vg, go, gl, dog, block, L=2 * n, part=part, workspace=ws)
+    assert bd.bdlm_read_error(ws) == 6  # BDLM_ERR_DEVICE_CHECK
+
+
 def test_packed_documents(bd):
     block, H, Hk, d = 32, 4, 2, 128
     lens = [128, 64, 320, 192, 64]
