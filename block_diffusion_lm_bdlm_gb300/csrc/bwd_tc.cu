@@ -31,15 +31,18 @@
 //   warp  12    loader: TMA for K, V, Q, dO; plain loads for lse and D; 3-stage
 //               ring for the per-step inputs
 //   warp  13    TMEM owner and MMA issuer (one thread). Per step s it issues
-//              S^T(s), dP^T(s), dQ^T(s-1), then dV(s) and dK(s) once P/dS(s)
-//              is ready, so dQ^T(s-1) overlaps the P/dS work of step s.
+//              S^T(s+1) and dP^T(s+1) as soon as the P/dS warps have read
+//              S^T(s) and dP^T(s) out of TMEM, then dV(s) and dK(s) once
+//              P/dS(s) is done, then dQ^T(s): the next step's S^T and dP^T run
+//              on the tensor pipe while P/dS(s) computes.
 // TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
 // P^T [384,416) | dQ^T [416,480) | dS^T [480,512). dS^T in shared memory is
-// double buffered. Because P^T and dS^T do not alias S^T and dP^T, the only
-// per-step handshake on the MMA thread's critical path is P/dS (arrived
-// right after the TMEM stores); the shared-memory copy of dS^T has its own
-// barrier, needed only by dQ^T one step later; tcgen05 commit order covers
-// the rest (an MMA's commit also covers every MMA issued before it).
+// double buffered. Because P^T and dS^T do not alias S^T and dP^T, S^T and
+// dP^T are free once loaded (barrier B_LD); P^T and dS^T of step s+1 are
+// written only after dV(s) and dK(s) completed (the stage's B_QDE commit).
+// The shared-memory copy of dS^T has its own barrier, needed only by dQ^T;
+// tcgen05 commit order covers the rest (an MMA's commit also covers every MMA
+// issued before it).
 // Every mbarrier wait is bounded (2 s).
 #include <cuda.h>
 
@@ -75,8 +78,8 @@ constexpr int SM_STG = SM_S + 2 * kST;     // + buffer * kStg
 constexpr int kSmemBytes = SM_STG + 2 * kStg + 1024;
 
 enum : int {
-    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_SS = 10 /* x2, by step parity */, B_DQ = 12, B_DQF = 14,
-    B_COUNT = 16
+    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_SS = 10 /* x2, by step parity */, B_DQ = 12, B_DQF = 13,
+    B_LD = 14, B_COUNT = 15
 };
 
 struct StepInfo {
@@ -207,56 +210,66 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
     return true;
 }
 
-__device__ __forceinline__ void issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
-                                         volatile int* abort, bool* ok) {
+__device__ __forceinline__ bool issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
+                                         volatile int* abort) {
     constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
     // dQ^T of the previous step must have been read out of TMEM, and this
-    // step's dS^T must be in shared memory
-    if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) { *ok = false; return; }
-    // (one barrier per step parity: the P/dS warps can finish the next step
-    // before this wait, but not the one after, which needs an S^T issued later)
-    if (!mma_wait(bar, B_SS + (ts & 1), (ts >> 1) & 1, abort)) { *ok = false; return; }
+    // step's dS^T must be in shared memory (one barrier per step parity: the
+    // P/dS warps cannot get two steps ahead, the step after next needs a
+    // dP^T that is issued after this dQ^T)
+    if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) return false;
+    if (!mma_wait(bar, B_SS + (ts & 1), (ts >> 1) & 1, abort)) return false;
     const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + (ts & 1) * kST;
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k)
         tc::mma_ss(tmem + TDQ, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
                    id_dq, k > 0);
     tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
+    return true;
 }
 
+// S^T = K Q^T and dP^T = V dO^T of global step ts, once its Q and dO are in shared memory.
+__device__ __forceinline__ bool issue_sdp(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts,
+                                          volatile int* abort) {
+    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // A, B K-major
+    const uint32_t st = ts % kStages;
+    if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return false;
+    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V;
+    const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
+        tc::mma_ss(tmem + TS, tc::sdesc_sw128(sK + oa, 16, 1024), tc::sdesc_sw128(sQ + ob, 16, 1024), id_st, k > 0);
+    }
+    tc::mma_commit(tc::smem_addr(&bar[B_S]));
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
+        tc::mma_ss(tmem + TDP, tc::sdesc_sw128(sV + oa, 16, 1024), tc::sdesc_sw128(sO + ob, 16, 1024), id_st, k > 0);
+    }
+    tc::mma_commit(tc::smem_addr(&bar[B_DP]));
+    return true;
+}
+
+// Per step s the tensor pipe receives S^T(s+1), dP^T(s+1), dV(s), dK(s),
+// dQ^T(s): the next step's S^T and dP^T go in as soon as the P/dS warps have
+// read S^T(s) and dP^T(s) into registers (B_LD), so they run while P/dS(s) is
+// still computing; dV(s) and dK(s) wait for P^T(s) and dS^T(s) (B_SM).
 __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
                                            uint32_t ts_base, uint32_t item_count, volatile int* abort) {
-    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // S^T, dP^T: A, B K-major
-    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);   // dV, dK: A K-major (TMEM / smem), B MN-major
+    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);  // dV, dK: A K-major (TMEM), B MN-major
     if (!mma_wait(bar, B_KV, item_count & 1, abort)) return;
-    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V;
-    bool ok = true;
+    if (c.n_steps == 0) return;
+    if (!issue_sdp(sbase, bar, tmem, ts_base, abort)) return;
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
-        if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return;
-        const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
-        // S^T = K Q^T. P/dS of the previous step has read S^T and dP^T (the
-        // MMAs of that step were issued after its B_SM), and P^T lives apart.
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-            const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-            tc::mma_ss(tmem + TS, tc::sdesc_sw128(sK + oa, 16, 1024), tc::sdesc_sw128(sQ + ob, 16, 1024), id_st, k > 0);
-        }
-        tc::mma_commit(tc::smem_addr(&bar[B_S]));
-        // dP^T = V dO^T
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-            const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-            tc::mma_ss(tmem + TDP, tc::sdesc_sw128(sV + oa, 16, 1024), tc::sdesc_sw128(sO + ob, 16, 1024), id_st, k > 0);
-        }
-        tc::mma_commit(tc::smem_addr(&bar[B_DP]));
-        // dQ^T of the previous step fills the gap while P/dS of this step is computed
-        if (s > 0) {
-            issue_dq(sbase, bar, tmem, ts - 1, s - 1, abort, &ok);
-            if (!ok) return;
+        if (s + 1 < c.n_steps) {
+            if (!mma_wait(bar, B_LD, ts & 1, abort)) return;
+            if (!issue_sdp(sbase, bar, tmem, ts + 1, abort)) return;
         }
         if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
         // dV += P^T dO, dK += dS^T Q (P^T and dS^T in TMEM)
+        const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
             tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
@@ -266,8 +279,8 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
             tc::mma_ts(tmem + TDK, tmem + TDS + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
                        (s > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
+        if (!issue_dq(sbase, bar, tmem, ts, s, abort)) return;
     }
-    if (c.n_steps > 0) issue_dq(sbase, bar, tmem, ts_base + c.n_steps - 1, c.n_steps - 1, abort, &ok);
 }
 
 // ------------------------------------------------------------ P/dS group
@@ -305,6 +318,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         const float4* lse4 = reinterpret_cast<const float4*>(info[st].nl2 + 32 * g);
         const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 32 * g);
         tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_LD]));  // S^T and dP^T of the next step may go
         uint32_t pp[16], dd[16];
         const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
@@ -325,6 +340,13 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
                 pp[2 * q + u] = pack2(p.x, p.y);
                 dd[2 * q + u] = pack2(ds.x, ds.y);
             }
+        }
+        // P^T and dS^T of the previous step must have been read by its dV and dK
+        if (ts > 0) {
+            const uint32_t tp = ts - 1;
+            got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + tp % kStages]), (tp / kStages) & 1, abort, kTimeoutNs);
+            if (!__all_sync(0xffffffffu, got)) return;
+            tc::tc_fence_after();
         }
         tc::tmem_st16(tmem + lb + TP + 16 * g, pp);
         tc::tmem_st16(tmem + lb + TDS + 16 * g, dd);
@@ -447,10 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(tc::smem_addr(&bar[B_SM]), 256);
         tc::mbar_init(tc::smem_addr(&bar[B_SS]), 256);
         tc::mbar_init(tc::smem_addr(&bar[B_SS + 1]), 256);
-        for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(tc::smem_addr(&bar[B_DQ + b]), 1);
-            tc::mbar_init(tc::smem_addr(&bar[B_DQF + b]), 1);
-        }
+        tc::mbar_init(tc::smem_addr(&bar[B_DQ]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 1);
+        tc::mbar_init(tc::smem_addr(&bar[B_LD]), 256);
         tc::fence_barrier_init();
     }
     if (warp == 13) {
