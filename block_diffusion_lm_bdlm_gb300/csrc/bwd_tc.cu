@@ -210,7 +210,29 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
     return true;
 }
 
-__device__ __forceinline__ bool issue_dq(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
+// Shared-memory descriptors of the operand tiles at stage / buffer 0. The
+// start address is the descriptor's low field (address >> 4, 14 bits), so a
+// tile at a byte offset is the base descriptor plus offset >> 4: the MMA
+// thread adds constants instead of rebuilding descriptors.
+struct Descs {
+    uint64_t k_km, v_km, q_km, o_km;  // K-major (S^T, dP^T operands)
+    uint64_t k_mn, s_mn, q_mn, o_mn;  // MN-major (dQ^T, dK, dV operands)
+};
+__device__ __forceinline__ Descs make_descs(uint32_t sbase) {
+    Descs d;
+    d.k_km = tc::sdesc_sw128(sbase + SM_K, 16, 1024);
+    d.v_km = tc::sdesc_sw128(sbase + SM_V, 16, 1024);
+    d.q_km = tc::sdesc_sw128(sbase + SM_Q, 16, 1024);
+    d.o_km = tc::sdesc_sw128(sbase + SM_O, 16, 1024);
+    d.k_mn = tc::sdesc_sw128(sbase + SM_K, kKV / 2, 1024);
+    d.s_mn = tc::sdesc_sw128(sbase + SM_S, kKV / 2, 1024);
+    d.q_mn = tc::sdesc_sw128(sbase + SM_Q, kQT / 2, 1024);
+    d.o_mn = tc::sdesc_sw128(sbase + SM_O, kQT / 2, 1024);
+    return d;
+}
+__device__ __forceinline__ uint64_t at(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+__device__ __forceinline__ bool issue_dq(const Descs& dd, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
                                          volatile int* abort) {
     constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
     // dQ^T of the previous step must have been read out of TMEM, and this
@@ -219,33 +241,30 @@ __device__ __forceinline__ bool issue_dq(uint32_t sbase, const uint64_t* bar, ui
     // dP^T that is issued after this dQ^T)
     if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) return false;
     if (!mma_wait(bar, B_SS + (ts & 1), (ts >> 1) & 1, abort)) return false;
-    const uint32_t sK = sbase + SM_K, sS = sbase + SM_S + (ts & 1) * kST;
+    const uint64_t sS = at(dd.s_mn, (ts & 1) * kST);
 #pragma unroll
-    for (int k = 0; k < BN / 16; ++k)
-        tc::mma_ss(tmem + TDQ, tc::sdesc_sw128(sK + 2048 * k, kKV / 2, 1024), tc::sdesc_sw128(sS + 2048 * k, kKV / 2, 1024),
-                   id_dq, k > 0);
+    for (int k = 0; k < BN / 16; ++k) tc::mma_ss(tmem + TDQ, at(dd.k_mn, 2048 * k), at(sS, 2048 * k), id_dq, k > 0);
     tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
     return true;
 }
 
 // S^T = K Q^T and dP^T = V dO^T of global step ts, once its Q and dO are in shared memory.
-__device__ __forceinline__ bool issue_sdp(uint32_t sbase, const uint64_t* bar, uint32_t tmem, uint32_t ts,
+__device__ __forceinline__ bool issue_sdp(const Descs& dd, const uint64_t* bar, uint32_t tmem, uint32_t ts,
                                           volatile int* abort) {
     constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // A, B K-major
     const uint32_t st = ts % kStages;
     if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return false;
-    const uint32_t sK = sbase + SM_K, sV = sbase + SM_V;
-    const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
+    const uint64_t q = at(dd.q_km, st * kQT), o = at(dd.o_km, st * kQT);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-        tc::mma_ss(tmem + TS, tc::sdesc_sw128(sK + oa, 16, 1024), tc::sdesc_sw128(sQ + ob, 16, 1024), id_st, k > 0);
+        tc::mma_ss(tmem + TS, at(dd.k_km, oa), at(q, ob), id_st, k > 0);
     }
     tc::mma_commit(tc::smem_addr(&bar[B_S]));
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-        tc::mma_ss(tmem + TDP, tc::sdesc_sw128(sV + oa, 16, 1024), tc::sdesc_sw128(sO + ob, 16, 1024), id_st, k > 0);
+        tc::mma_ss(tmem + TDP, at(dd.v_km, oa), at(o, ob), id_st, k > 0);
     }
     tc::mma_commit(tc::smem_addr(&bar[B_DP]));
     return true;
@@ -260,26 +279,25 @@ __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, con
     constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);  // dV, dK: A K-major (TMEM), B MN-major
     if (!mma_wait(bar, B_KV, item_count & 1, abort)) return;
     if (c.n_steps == 0) return;
-    if (!issue_sdp(sbase, bar, tmem, ts_base, abort)) return;
+    const Descs dd = make_descs(sbase);
+    if (!issue_sdp(dd, bar, tmem, ts_base, abort)) return;
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
         if (s + 1 < c.n_steps) {
             if (!mma_wait(bar, B_LD, ts & 1, abort)) return;
-            if (!issue_sdp(sbase, bar, tmem, ts + 1, abort)) return;
+            if (!issue_sdp(dd, bar, tmem, ts + 1, abort)) return;
         }
         if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
         // dV += P^T dO, dK += dS^T Q (P^T and dS^T in TMEM)
-        const uint32_t sQ = sbase + SM_Q + st * kQT, sO = sbase + SM_O + st * kQT;
+        const uint64_t q = at(dd.q_mn, st * kQT), o = at(dd.o_mn, st * kQT);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, tc::sdesc_sw128(sO + 2048 * k, kQT / 2, 1024), id_kv,
-                       (s > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, at(o, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDK, tmem + TDS + 8 * k, tc::sdesc_sw128(sQ + 2048 * k, kQT / 2, 1024), id_kv,
-                       (s > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(tmem + TDK, tmem + TDS + 8 * k, at(q, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
-        if (!issue_dq(sbase, bar, tmem, ts, s, abort)) return;
+        if (!issue_dq(dd, bar, tmem, ts, s, abort)) return;
     }
 }
 
