@@ -120,17 +120,21 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
     if (!tc::mbar_wait(tc::smem_addr(&bar[B_Q]), q_count & 1, abort, kTimeoutNs)) return;
     tc::tc_fence_after();
     const int nh = c.two ? 2 : 1;
+    // operand descriptors of the shared-memory base, K-major (Q, K) and
+    // MN-major (V); tiles, K slices and stages are constant offsets
+    const uint64_t km = tc::sdesc_sw128(sbase, 16, 1024);
+    const uint64_t mn = tc::sdesc_sw128(sbase, S::kChunk, 1024);
     for (int j = 0; j < c.nk; ++j) {
         const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
         if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + s]), ph, abort, kTimeoutNs)) return;
         tc::tc_fence_after();
-        const uint32_t sK = sbase + S::kK + s * S::kTile;
+        const uint64_t dK = tc::sdesc_add(km, S::kK + s * S::kTile);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             if (i >= nh) break;
             const uint32_t ti = i == 0 ? t : t_base1 + j;
             const uint32_t tS = tmem + 128 * i;
-            const uint32_t sQ = sbase + (i == 0 ? S::kQ0 : S::kQ1);
+            const uint64_t dQ = tc::sdesc_add(km, i == 0 ? S::kQ0 : S::kQ1);
             if (j > 0) {  // O_i += P_i V of the previous tile has read P_i
                 if (!tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), (ti - 1) & 1, abort, kTimeoutNs)) return;
                 tc::tc_fence_after();
@@ -138,13 +142,12 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = (k >> 2) * S::kChunk + (k & 3) * 32;
-                tc::mma_ss(tS, tc::sdesc_sw128(sQ + off, 16, 1024), tc::sdesc_sw128(sK + off, 16, 1024), idesc_s,
-                           k > 0);
+                tc::mma_ss(tS, tc::sdesc_add(dQ, off), tc::sdesc_add(dK, off), idesc_s, k > 0);
             }
             tc::mma_commit(tc::smem_addr(&bar[B_S + i]));
         }
         if (!tc::mbar_wait(tc::smem_addr(&bar[B_VFULL + s]), ph, abort, kTimeoutNs)) return;
-        const uint32_t sV = sbase + S::kV + s * S::kTile;
+        const uint64_t dV = tc::sdesc_add(mn, S::kV + s * S::kTile);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             if (i >= nh) break;
@@ -156,13 +159,12 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
             tc::tc_fence_after();
 #pragma unroll
             for (int k = 0; k < BN / 32; ++k)
-                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o,
-                           (j > 0 || k > 0) ? 1u : 0u);
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
             if (!tc::mbar_wait(tc::smem_addr(&bar[B_P + i]), ti & 1, abort, kTimeoutNs)) return;
             tc::tc_fence_after();
 #pragma unroll
             for (int k = BN / 32; k < BN / 16; ++k)
-                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_sw128(sV + 2048 * k, S::kChunk, 1024), idesc_o, 1u);
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, 1u);
             tc::mma_commit(tc::smem_addr(&bar[B_O + i]));
         }
         tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));

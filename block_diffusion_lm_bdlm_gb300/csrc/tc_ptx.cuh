@@ -159,6 +159,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The descriptor of the tile `bytes` further on in shared memory: the start
+// address is the descriptor's low field (address >> 4, 14 bits), so an offset
+// that keeps the address below 256 KB adds directly. The MMA issuers build
+// each tile's descriptor once and step through K slices and stages with this.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
 // A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
