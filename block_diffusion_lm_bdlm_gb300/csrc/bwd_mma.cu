@@ -14,7 +14,8 @@
 //      accumulates dV += P^T dO and dK += dS^T Q in registers (no atomics:
 //      the item owns its keys for all G heads), and adds dq += dS K into the
 //      fp32 accumulator with vector atomics;
-//   3. convert: dq = bf16(accumulator).
+//   3. convert: dq = bf16(accumulator), times the softmax scale when the
+//      main kernel accumulated dS K unscaled (the tensor-core kernel).
 #include <climits>
 
 #include "common.cuh"
@@ -65,17 +66,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdArgs a) {
+// dq = bf16(mul * accumulator): the tensor-core main kernel accumulates
+// dS K unscaled (mul = softmax scale), the warp-level one scaled (mul = 1).
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdArgs a, float mul) {
     const long long i = (long long)blockIdx.x * 256 + threadIdx.x;  // 8 elements each
     const long long n = a.Lq * a.H * D / 8;
     if (i >= n) return;
     const float4 x = reinterpret_cast<const float4*>(a.dqacc)[2 * i];
     const float4 y = reinterpret_cast<const float4*>(a.dqacc)[2 * i + 1];
     uint4 out;
-    out.x = pack_bf16(x.x, x.y);
-    out.y = pack_bf16(x.z, x.w);
-    out.z = pack_bf16(y.x, y.y);
-    out.w = pack_bf16(y.z, y.w);
+    out.x = pack_bf16(x.x * mul, x.y * mul);
+    out.y = pack_bf16(x.z * mul, x.w * mul);
+    out.z = pack_bf16(y.x * mul, y.y * mul);
+    out.w = pack_bf16(y.z * mul, y.w * mul);
     reinterpret_cast<uint4*>(a.dq)[i] = out;
 }
 
@@ -302,7 +305,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (D == 128) {
+    if constexpr (D == 128) {
         e = launch_bwd_tc_main(a, num_sms, st);  // tensor-core main kernel, 128-key tiles
     } else {
         constexpr int smem = bwd_smem_bytes<D>();
@@ -313,7 +316,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
     }
     if (e != cudaSuccess) return e;
     const long long cv = pairs * D / 8;
-    bwd_convert_kernel<D><<<(unsigned)((cv + 255) / 256), 256, 0, st>>>(a);
+    bwd_convert_kernel<D><<<(unsigned)((cv + 255) / 256), 256, 0, st>>>(a, D == 128 ? a.scale : 1.f);
     return cudaGetLastError();
 }
 

@@ -210,10 +210,9 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
     return true;
 }
 
-// Shared-memory descriptors of the operand tiles at stage / buffer 0. The
-// start address is the descriptor's low field (address >> 4, 14 bits), so a
-// tile at a byte offset is the base descriptor plus offset >> 4: the MMA
-// thread adds constants instead of rebuilding descriptors.
+// Shared-memory descriptors of the operand tiles at stage / buffer 0; the MMA
+// thread steps to K slices, stages and buffers with tc::sdesc_add instead of
+// rebuilding descriptors.
 struct Descs {
     uint64_t k_km, v_km, q_km, o_km;  // K-major (S^T, dP^T operands)
     uint64_t k_mn, s_mn, q_mn, o_mn;  // MN-major (dQ^T, dK, dV operands)
@@ -230,7 +229,7 @@ __device__ __forceinline__ Descs make_descs(uint32_t sbase) {
     d.o_mn = tc::sdesc_sw128(sbase + SM_O, kQT / 2, 1024);
     return d;
 }
-__device__ __forceinline__ uint64_t at(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+__device__ __forceinline__ uint64_t at(uint64_t desc, uint32_t bytes) { return tc::sdesc_add(desc, bytes); }
 
 __device__ __forceinline__ bool issue_dq(const Descs& dd, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
                                          volatile int* abort) {
@@ -412,9 +411,9 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
             // staging buffer `half` was last read by the reduce issued one step ago
             if (leader) bulk_wait_read1();
             named_sync(2, 128);
-            float* stg = reinterpret_cast<float*>(smem + SM_STG + half * kStg);
+            float* stg = reinterpret_cast<float*>(smem + SM_STG + half * kStg) + dl;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stg[e * D + dl] = __uint_as_float(qv[half][e]) * a.scale;
+            for (int e = 0; e < 32; ++e) stg[e * D] = __uint_as_float(qv[half][e]);  // scaled in the convert kernel
             tc::fence_proxy_async_smem();
             named_sync(2, 128);
             if (leader) {
