@@ -39,9 +39,11 @@ METRIC = "BDLM attn fwd+bwd TFLOP/s (valid pairs) and % BF16 peak at 128K, 1 GB3
 UNIT = "TFLOP/s"
 
 # dram traffic of the dominant kernel per launch from an ncu capture, valid
-# while its source is unchanged (checked by hash; otherwise reported as null)
-TRAFFIC = {"kernel_source": "block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu", "sha1": "3ea96ff18957bd4ff3a111ddab724e59838e04e4",
-           "bytes_per_launch": 334237201920 + 176170302464,
+# while the sources it is compiled from are unchanged (checked by hash;
+# otherwise reported as null)
+TRAFFIC = {"kernel_sources": ['block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu', 'block_diffusion_lm_bdlm_gb300/csrc/common.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/tc_ptx.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/kernels.h'],
+           "sha1": "5dd4721874e775c73ea176173abeb6ff4f326854",
+           "bytes_per_launch": 801709125888 + 406183671296,
            "note": "bwd_tc_kernel on this workload, ncu dram__bytes_read.sum + dram__bytes_write.sum"}
 
 
@@ -125,9 +127,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_sha(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+def source_sha(rels):
+    h = hashlib.sha1()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # ----------------------------------------------------------------------------
@@ -432,7 +437,7 @@ def l2_note(x):
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks):
     traffic = None
-    if TRAFFIC["sha1"] and TRAFFIC["kernel_source"] and source_sha(TRAFFIC["kernel_source"]) == TRAFFIC["sha1"]:
+    if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
     mbytes = merge_bytes(w, len(step.windows))
     out = {
