@@ -30,6 +30,7 @@ __all__ = [
 BDLM_OK = 0
 BDLM_BF16, BDLM_F32 = 0, 1
 PART_NONE, PART_KEY_WINDOW, PART_BLOCK_GROUP = 0, 1, 2
+PART_ACCUMULATE = 1
 
 EXPORTED_SYMBOLS = (
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_attn_fwd", "bdlm_attn_bwd",
@@ -46,37 +47,44 @@ class BDLMError(RuntimeError):
 
 class _CPartial(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("n_q_blocks", ctypes.c_int32), ("key_lo", ctypes.c_int64),
-                ("key_hi", ctypes.c_int64), ("q_blocks", ctypes.c_void_p)]
+                ("key_hi", ctypes.c_int64), ("q_blocks", ctypes.c_void_p), ("flags", ctypes.c_int32),
+                ("o_dtype", ctypes.c_int32)]
 
 
 @dataclass
 class Partial:
-    """Restriction of a forward call (see bdlm_partial in include/bdlm.h).
+    """Restriction of a call (see bdlm_partial in include/bdlm.h).
 
     Partial.window(lo, hi): k/v hold the keys at positions [lo, hi).
+    Partial.window(lo, hi, accumulate=True): forward only; `out` and `lse`
+        hold the merged result of earlier windows and this call merges in.
     Partial.group(blocks): q holds the corrupted rows of `blocks` (device int32).
+    The element type of a partial forward's o follows the `out` tensor (bf16
+    or fp32).
     """
     kind: int
     key_lo: int = 0
     key_hi: int = 0
     q_blocks: Optional[torch.Tensor] = None
+    accumulate: bool = False
 
     @staticmethod
-    def window(lo: int, hi: int) -> "Partial":
-        return Partial(PART_KEY_WINDOW, key_lo=int(lo), key_hi=int(hi))
+    def window(lo: int, hi: int, accumulate: bool = False) -> "Partial":
+        return Partial(PART_KEY_WINDOW, key_lo=int(lo), key_hi=int(hi), accumulate=bool(accumulate))
 
     @staticmethod
     def group(blocks: torch.Tensor) -> "Partial":
         return Partial(PART_BLOCK_GROUP, q_blocks=blocks)
 
-    def c(self) -> _CPartial:
+    def c(self, o_dtype: int = 0) -> _CPartial:
         nb, ptr = 0, None
         if self.kind == PART_BLOCK_GROUP:
             b = self.q_blocks
             if b is None or b.dtype != torch.int32 or not b.is_cuda or not b.is_contiguous():
                 raise ValueError("q_blocks must be a contiguous int32 CUDA tensor")
             nb, ptr = b.numel(), b.data_ptr()
-        return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr)
+        flags = PART_ACCUMULATE if self.accumulate else 0
+        return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr, flags, o_dtype)
 
 
 _lib = None
@@ -156,11 +164,31 @@ def bdlm_last_launch_count() -> int:
     return int(load_library().bdlm_last_launch_count())
 
 
+def _fwd_outputs(q, part, out, lse):
+    """Allocate or check the forward's o and lse; returns (out, lse, o_dtype)."""
+    Lq, H, d = q.shape
+    if part is not None and part.accumulate and (out is None or lse is None):
+        raise ValueError("an accumulating window needs the running `out` and `lse`")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, Lq), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (Lq, H, d) or not out.is_cuda \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 or fp32 CUDA tensor shaped like q")
+    if out.dtype == torch.float32 and part is None:
+        raise ValueError("fp32 o is for partial calls; full attention writes bf16")
+    if tuple(lse.shape) != (H, Lq) or lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [H, Lq]")
+    return out, lse, (BDLM_F32 if out.dtype == torch.float32 else BDLM_BF16)
+
+
 def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=None, softmax_scale: float = 0.0,
                   part: Optional[Partial] = None, out=None, lse=None, workspace=None, stream=None):
     """BDLM attention forward. q [Lq,H,d], k/v [Lk,Hk,d] bf16 CUDA tensors.
     L defaults to q's rows (full attention, key window) and must be given as
-    2n for a block group. Returns (o [Lq,H,d] bf16, lse [H,Lq] fp32)."""
+    2n for a block group. Returns (o [Lq,H,d], lse [H,Lq] fp32); o is bf16
+    unless a partial call is given an fp32 `out`."""
     lib = load_library()
     for nm, t in (("q", q), ("k", k), ("v", v)):
         _bf16_cuda(nm, t)
@@ -168,14 +196,11 @@ def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=No
     Hk = k.shape[1]
     L = Lq if L is None else int(L)
     cu_ptr, n_docs = _cu(cu_seqlens)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((H, Lq), dtype=torch.float32, device=q.device)
+    out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
     ws_bytes = lib.bdlm_attn_fwd_workspace_bytes(L, H, d, n_docs)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
-    cpart = ctypes.byref(part.c()) if part is not None else None
+    cpart = ctypes.byref(part.c(o_dtype)) if part is not None else None
     st = lib.bdlm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L, block, H,
                            Hk, d, cu_ptr, n_docs, softmax_scale, cpart, workspace.data_ptr(),
                            workspace.numel(), _stream(stream))
@@ -197,11 +222,8 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
     Hk = k.shape[1]
     L = Lq if L is None else int(L)
     cu_ptr, n_docs = _cu(cu_seqlens)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((H, Lq), dtype=torch.float32, device=q.device)
-    cpart = ctypes.byref(part.c()) if part is not None else None
+    out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
+    cpart = ctypes.byref(part.c(o_dtype)) if part is not None else None
     st = lib.bdlm_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L,
                                    block, H, Hk, d, cu_ptr, n_docs, softmax_scale, cpart, _stream(stream))
     _check(st, "bdlm_attn_fwd_noalloc")

@@ -167,6 +167,13 @@ int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
     int st = check_common(q, k, v, L, block, heads, kv_heads, head_dim, cu_seqlens, n_docs, part, &lay, &cm);
     if (st != BDLM_OK) return st;
     if (!o || !lse || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return BDLM_ERR_INVALID_ARG;
+    const int kind = part ? part->kind : BDLM_PART_NONE;
+    const int flags = part ? part->flags : 0;
+    const int o_dtype = part ? part->o_dtype : BDLM_BF16;
+    if (flags & ~BDLM_PART_ACCUMULATE) return BDLM_ERR_INVALID_ARG;
+    if ((flags & BDLM_PART_ACCUMULATE) && kind != BDLM_PART_KEY_WINDOW) return BDLM_ERR_INVALID_ARG;
+    if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return BDLM_ERR_INVALID_ARG;
+    if (o_dtype == BDLM_F32 && kind == BDLM_PART_NONE) return BDLM_ERR_INVALID_ARG;
     const int docs = cu_seqlens ? n_docs : 1;
     if (!workspace || !aligned256(workspace)) return BDLM_ERR_WORKSPACE;
     if (workspace_bytes < bdlm_attn_fwd_workspace_bytes(L, heads, head_dim, docs)) return BDLM_ERR_WORKSPACE;
@@ -183,8 +190,10 @@ int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.k = static_cast<const __nv_bfloat16*>(k);
     a.v = static_cast<const __nv_bfloat16*>(v);
-    a.o = static_cast<__nv_bfloat16*>(o);
+    a.o = o_dtype == BDLM_F32 ? nullptr : static_cast<__nv_bfloat16*>(o);
+    a.o_f32 = o_dtype == BDLM_F32 ? static_cast<float*>(o) : nullptr;
     a.lse = lse;
+    a.accumulate = (flags & BDLM_PART_ACCUMULATE) ? 1 : 0;
     a.lay = lay;
     a.H = heads;
     a.Hk = kv_heads;
@@ -209,6 +218,7 @@ int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
     Common cm{};
     int st = check_common(q, k, v, L, block, heads, kv_heads, head_dim, cu_seqlens, n_docs, part, &lay, &cm);
     if (st != BDLM_OK) return st;
+    if (part && (part->flags != 0 || part->o_dtype != BDLM_BF16)) return BDLM_ERR_INVALID_ARG;  // forward-only fields
     if (!o || !lse || !dO || !dq || !dk || !dv) return BDLM_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))

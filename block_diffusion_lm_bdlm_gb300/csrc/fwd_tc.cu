@@ -272,9 +272,28 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         tc::tc_fence_after();
     }
     const bool have_o = ok && c.nk > 0;  // warp-uniform
-    const float inv = l > 0.f ? 1.f / l : 0.f;
     const bool store = row < c.T.nrows;
-    __nv_bfloat16* orow = a.o + ((long long)c.q_row0 + row) * ((long long)a.H * D) + (long long)h * D;
+    const long long ooff = ((long long)c.q_row0 + row) * ((long long)a.H * D) + (long long)h * D;
+    const long long lidx = (long long)h * a.Lq + c.q_row0 + row;
+    // this call's row: lse in base 2, o = (unnormalised O) * cw
+    const float l2w = l > 0.f ? m_use + __log2f(l) : -INFINITY;
+    float cw = l > 0.f ? 1.f / l : 0.f, ca = 0.f, l2out = l2w;
+    bool write = store;
+    if (a.accumulate && store) {
+        // running merge with the stored result of earlier windows (log-sum-exp
+        // weights in fp32); a window the row cannot see leaves it unchanged
+        const float l2a = a.lse[lidx] * 1.4426950408889634f;
+        if (l2w == -INFINITY) {
+            write = false;
+        } else if (l2a != -INFINITY) {
+            const float mx = fmaxf(l2a, l2w);
+            const float wa = ex2f(l2a - mx), ww = ex2f(l2w - mx);
+            const float rz = 1.f / (wa + ww);
+            ca = wa * rz;
+            cw *= ww * rz;
+            l2out = mx + __log2f(wa + ww);
+        }
+    }
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
@@ -285,22 +304,45 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+        if (!write) continue;
+        float v[32];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float* f = reinterpret_cast<const float*>(&o[8 * e]);
-                dst[e] = make_uint4(pack2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
-                                    pack2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
-                                    pack2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
-                                    pack2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
-                (void)f;
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * cw;
+        if (a.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(a.o_f32 + ooff + 32 * q);
+            if (ca != 0.f) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 t = dst[e];
+                    v[4 * e] = fmaf(ca, t.x, v[4 * e]);
+                    v[4 * e + 1] = fmaf(ca, t.y, v[4 * e + 1]);
+                    v[4 * e + 2] = fmaf(ca, t.z, v[4 * e + 2]);
+                    v[4 * e + 3] = fmaf(ca, t.w, v[4 * e + 3]);
+                }
             }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(a.o + ooff + 32 * q);
+            if (ca != 0.f) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint4 t = dst[e];
+                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[8 * e + 2 * u] = fmaf(ca, __uint_as_float(w[u] << 16), v[8 * e + 2 * u]);
+                        v[8 * e + 2 * u + 1] = fmaf(ca, __uint_as_float(w[u] & 0xffff0000u), v[8 * e + 2 * u + 1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pack2(v[8 * e], v[8 * e + 1]), pack2(v[8 * e + 2], v[8 * e + 3]),
+                                    pack2(v[8 * e + 4], v[8 * e + 5]), pack2(v[8 * e + 6], v[8 * e + 7]));
         }
     }
-    if (store)
-        a.lse[(long long)h * a.Lq + c.q_row0 + row] =
-            l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (write) a.lse[lidx] = l2out == -INFINITY ? -INFINITY : l2out * 0.69314718055994531f;
 }
 
 // ------------------------------------------------------------------ kernel

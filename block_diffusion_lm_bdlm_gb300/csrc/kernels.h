@@ -22,8 +22,10 @@ struct FwdArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
-    __nv_bfloat16* o;
+    __nv_bfloat16* o;   // bf16 output (o_f32 == nullptr)
+    float* o_f32;       // fp32 output of a partial (o == nullptr)
     float* lse;
+    int accumulate;     // merge into the running (o, lse) instead of overwriting
     Layout lay;
     int H, Hk, G, D;
     float scale_log2;  // softmax scale * log2(e)

@@ -67,8 +67,12 @@ enum bdlm_part_kind {
     BDLM_PART_BLOCK_GROUP = 2  /* queries restricted to a list of corrupted blocks*/
 };
 
+enum bdlm_part_flags {
+    BDLM_PART_ACCUMULATE = 1   /* KEY_WINDOW forward: merge into the running o, lse */
+};
+
 /*
- * Restriction of one forward call (single sequence only; cu_seqlens == NULL).
+ * Restriction of one call (single sequence only; cu_seqlens == NULL).
  *
  * BDLM_PART_KEY_WINDOW - partial attention against one shard of the keys, as
  *   each rank computes it under context-sharded block parallelism (Block
@@ -84,12 +88,29 @@ enum bdlm_part_kind {
  *   (Lq = n_q_blocks * B). k and v hold the n clean rows followed by the same
  *   blocks' corrupted rows in the same order (Lk = n + n_q_blocks * B).
  *   q_blocks is a DEVICE array of distinct block ids in [0, n / B).
+ *
+ * flags (forward only):
+ *   BDLM_PART_ACCUMULATE - KEY_WINDOW only. o and lse already hold the merged
+ *   result of earlier windows of the same query rows (disjoint key sets), and
+ *   this call merges its window into them in place with log-sum-exp weights,
+ *   in fp32 ("Block Parallelism ..." abstract: sharding the clean sequence
+ *   keeps the result; rit.work CSBP post, CSBP paragraph): lse = ln(e^lse +
+ *   e^lse_w), o = (e^lse o + e^lse_w o_w) / (e^lse + e^lse_w). Rows that see no
+ *   key of the window are left unchanged; rows whose running lse is -inf take
+ *   the window's result (their o is not read). The first window of a sequence
+ *   is an ordinary call without the flag. This replaces storing every window's
+ *   partial and one bdlm_lse_merge call.
+ * o_dtype: BDLM_BF16 (0, default) or BDLM_F32 - the element type of o for a
+ *   KEY_WINDOW or BLOCK_GROUP forward (fp32 keeps a running merge from being
+ *   rounded at every window). Full attention and the backward take bf16 o.
  */
 typedef struct {
     int32_t kind;            /* enum bdlm_part_kind                               */
     int32_t n_q_blocks;      /* BLOCK_GROUP: number of listed blocks              */
     int64_t key_lo, key_hi;  /* KEY_WINDOW: sequence positions, 0<=lo<hi<=L       */
     const int32_t* q_blocks; /* BLOCK_GROUP: device int32 [n_q_blocks]            */
+    int32_t flags;           /* enum bdlm_part_flags (0 = none)                   */
+    int32_t o_dtype;         /* enum bdlm_dtype of o (forward partials)           */
 } bdlm_partial;
 
 /* Workspace sizes (bytes) for one call with L query rows, H heads, head dim d

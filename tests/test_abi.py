@@ -97,6 +97,14 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, part=ctypes.byref(p)) == INVALID
     p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None)
     assert _fwd(lib, part=ctypes.byref(p), cu=256, n_docs=1) == UNSUP  # windows need one sequence
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 1, 0, 0, 16, bd.PART_ACCUMULATE, 0)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # only key windows accumulate
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, 4, 0)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # unknown flag
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, 0, 7)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # unknown o dtype
+    p = bd._CPartial(bd.PART_NONE, 0, 0, 0, None, 0, bd.BDLM_F32)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # fp32 o is for partials
     assert lib.bdlm_last_launch_count() == 0
 
 
@@ -113,6 +121,8 @@ def test_backward_and_merge_reject_bad_arguments(lib):
     assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 257, None)) == 1        # past the sequence
     assert bwd(bd._CPartial(bd.PART_BLOCK_GROUP, 0, 0, 0, None)) == 1         # no block list
     assert bwd(bd._CPartial(bd.PART_BLOCK_GROUP, 9, 0, 0, 16)) == 1           # more blocks than n / B
+    assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, bd.PART_ACCUMULATE, 0)) == 1  # forward-only flag
+    assert bwd(bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, 0, bd.BDLM_F32)) == 1         # bf16 o only
     st = lib.bdlm_attn_bwd(16, 16, 16, 16, 16, None, 16, 16, 16, 256, 16, 2, 2, 64, None, 1, 0.0, None, 256,
                            1 << 20, None)
     assert st == 1

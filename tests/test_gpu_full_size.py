@@ -105,6 +105,17 @@ def test_long128k_sharded_forward_merge_backward(bd):
     assert (o.float() - uo.float()).abs().max().item() <= 2e-2
     assert ((lse - ul).abs() / ul.abs().clamp(min=1.0)).max().item() <= 1e-3
     del uo, ul
+    # the same windows merged into a running fp32 (o, lse) by the forward's
+    # epilogue == the merge kernel's result
+    ro = torch.empty(x.q.shape, dtype=torch.float32, device="cuda")
+    rl = torch.empty_like(lse)
+    for i, (lo, hi) in enumerate(windows):
+        bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], B, part=bd.Partial.window(lo, hi, accumulate=i > 0), out=ro,
+                         lse=rl, workspace=wsf)
+    assert bd.bdlm_read_error(wsf) == 0
+    assert (ro - o.float()).abs().max().item() <= 2e-2
+    assert ((rl - lse).abs() / lse.abs().clamp(min=1.0)).max().item() <= 1e-3
+    del ro, rl
     nb = n // B
     blocks = [(0, 0), (0, (nb // 2) * B), (0, (nb - 1) * B), (0, n), (0, n + (nb // 3) * B), (0, n + (nb - 1) * B)]
     sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 7], blocks=blocks)

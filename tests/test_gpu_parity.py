@@ -172,6 +172,33 @@ def test_block_groups(bd, n, block, H, Hk, groups):
         assert (gl - lse[:, qi]).abs().max().item() <= 1e-3 * max(1.0, lse.abs().max().item())
 
 
+# running merge: each window merged into (o, lse) in the forward's epilogue
+@pytest.mark.parametrize("n,block,H,Hk,d,shards", [(256, 16, 2, 2, 64, 2), (320, 32, 8, 2, 128, 3),
+                                                   (96, 16, 4, 1, 128, 8)])
+@pytest.mark.parametrize("o_dtype", [torch.bfloat16, torch.float32])
+def test_running_merge_in_forward(bd, n, block, H, Hk, d, shards, o_dtype):
+    w, x = gen(n, block, H, Hk, d, seed=5 * n + shards)
+    full = oracle.bdlm_attention(host(x.q), host(x.k), host(x.v), block, w.scale)
+    windows = synth.shard_bounds(n, shards) + [(n, 2 * n)]
+    o = torch.empty(x.q.shape, dtype=o_dtype, device="cuda")
+    lse = torch.empty((H, 2 * n), dtype=torch.float32, device="cuda")
+    ws = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(2 * n, H, d, 1), dtype=torch.uint8, device="cuda")
+    for i, (lo, hi) in enumerate(windows):
+        prev_o, prev_l = o.clone(), lse.clone()
+        bd.bdlm_attn_fwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), block,
+                         part=bd.Partial.window(lo, hi, accumulate=i > 0), out=o, lse=lse, workspace=ws)
+        assert bd.bdlm_read_error(ws) == 0
+        if i > 0:
+            # rows that see no key of this window keep their running result bit for bit
+            pr = oracle.partial_attention(host(x.q), host(x.k)[lo:hi], host(x.v)[lo:hi], n, block, lo, hi, w.scale)
+            unseen = torch.from_numpy(np.isneginf(pr["lse"])).cuda()
+            assert torch.equal(lse[unseen], prev_l[unseen])
+            assert torch.equal(o.transpose(0, 1)[unseen], prev_o.transpose(0, 1)[unseen])
+    torch.cuda.synchronize()
+    check_o(host(o), full["o"], "running-merge o")
+    check_lse(host(lse), full["lse"], "running-merge lse")
+
+
 # sharded backward: each clean-K/V shard (and the local corrupted keys) with
 # the merged forward's o and lse; shares of dq sum to the full dq
 SHARDED = [

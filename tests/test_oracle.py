@@ -277,6 +277,32 @@ def test_merge_special_cases():
     np.testing.assert_allclose(l, l1 + math.log(2), atol=1e-14)
 
 
+@pytest.mark.parametrize("shards", [2, 3, 8])
+def test_running_merge_equals_one_shot_merge(shards):
+    # Merging window partials one at a time into a running (o, lse), as the
+    # forward's accumulate mode does, gives the one-shot merge (log-sum-exp
+    # merging is associative) and so the unsharded attention; a window a row
+    # cannot see (-inf partial) leaves the running row as it was.
+    n, block, H, Hk, d = 48, 8, 4, 2, 8
+    q, k, v, _ = case(n, block, H, Hk, d, seed=61)
+    scale = 0.3
+    windows = synth.shard_bounds(n, shards) + [(n, 2 * n)]
+    parts = [oracle.partial_attention(q, k[lo:hi], v[lo:hi], n, block, lo, hi, scale) for lo, hi in windows]
+    o, lse = parts[0]["o"], parts[0]["lse"]
+    for p in parts[1:]:
+        before_o, before_l = o, lse
+        o, lse = oracle.lse_merge([o, p["o"]], [lse, p["lse"]])
+        unseen = np.isneginf(p["lse"])
+        assert np.array_equal(lse[unseen], before_l[unseen])
+        assert np.array_equal(o[unseen.T], before_o[unseen.T])
+    o1, lse1 = oracle.lse_merge([p["o"] for p in parts], [p["lse"] for p in parts])
+    np.testing.assert_allclose(o, o1, atol=1e-12)
+    np.testing.assert_allclose(lse, lse1, atol=1e-12)
+    full = oracle.dense_bdlm_attention(q, k, v, n, block, scale)
+    np.testing.assert_allclose(o, full["o"], atol=1e-12)
+    np.testing.assert_allclose(lse, full["lse"], atol=1e-12)
+
+
 # --------------------------------------------------------------------------
 # early/late block groups == unsplit corrupted rows
 # --------------------------------------------------------------------------
