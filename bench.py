@@ -260,6 +260,31 @@ class Step:
             ev[3].record()
         self.launches += launches
 
+    def time_running_merge(self, reps=2):
+        """The same windows merged by the forward's epilogue into a running
+        fp32 (o, lse) instead of kept as partials and merged (not part of the
+        timed step). Returns the median ms of `reps` runs after one warm-up."""
+        bd, w, x = self.bd, self.w, self.x
+        ro = torch.empty(x.q.shape, dtype=torch.float32, device=x.q.device)
+        rl = torch.empty_like(self.lse)
+
+        def run():
+            for i, (lo, hi) in enumerate(self.windows):
+                bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], w.block, part=bd.Partial.window(lo, hi, accumulate=i > 0),
+                                 out=ro, lse=rl, workspace=self.ws_f)
+
+        run()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        del ro, rl
+        return statistics.median(times)
+
 
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -344,11 +369,12 @@ def run_cuda(args, rank, world, local):
     peaks, peak_kind = load_peaks()
     achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    run_ms = step.time_running_merge()
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks)
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -435,7 +461,7 @@ def l2_note(x):
 
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks):
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -459,6 +485,7 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "fwd_frac_bf16": f_fwd / (fwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
             "bwd_frac_bf16": f_bwd / (bwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
             "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
+            "fwd_running_merge_ms": run_ms, "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12,
         },
         "e2e": e2e,
         "gpu_launches": launches,

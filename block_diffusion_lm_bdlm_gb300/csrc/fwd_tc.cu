@@ -210,13 +210,14 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
             for (int e = 0; e < 128; ++e)
                 if (!rel_sees(ri, e)) x[e] = -INFINITY;
         }
+        // row max, four independent chains of three-input max
         float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-        for (int e = 4; e < 128; e += 4) {
-            mx0 = fmaxf(mx0, x[e]);
-            mx1 = fmaxf(mx1, x[e + 1]);
-            mx2 = fmaxf(mx2, x[e + 2]);
-            mx3 = fmaxf(mx3, x[e + 3]);
+        for (int e = 4; e < 128; e += 8) {
+            mx0 = tc::fmax3(mx0, x[e], x[e + 1]);
+            mx1 = tc::fmax3(mx1, x[e + 2], x[e + 3]);
+            mx2 = tc::fmax3(mx2, x[e + 4], x[e + 5]);
+            mx3 = tc::fmax3(mx3, x[e + 6], x[e + 7]);
         }
         const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         const bool move = mx > m_use + 8.0f;
@@ -238,15 +239,16 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
             }
         }
         const float m_eff = m_use == -INFINITY ? 0.f : m_use;
-        float s0 = 0.f, s1 = 0.f;
+        // p = exp2(x * scale * log2 e - m) on packed pairs; row sum in two lanes
+        const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m_eff, -m_eff);
+        float2 sum2 = make_float2(0.f, 0.f);
         uint32_t pa[32], pb[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2f(fmaf(x[2 * e], sl2, -m_eff));
-            const float p1 = ex2f(fmaf(x[2 * e + 1], sl2, -m_eff));
-            s0 += p0;
-            s1 += p1;
-            pa[e] = pack2(p0, p1);
+            const float2 y = tc::fma2(make_float2(x[2 * e], x[2 * e + 1]), sl2x2, nm2);
+            const float2 p = make_float2(ex2f(y.x), ex2f(y.y));
+            sum2 = tc::add2(sum2, p);
+            pa[e] = pack2(p.x, p.y);
         }
         tc::tmem_st32(tS, pa);
         tc::tmem_st_wait();
@@ -254,14 +256,13 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         tc::mbar_arrive(tc::smem_addr(&bar[B_PH + i]));
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2f(fmaf(x[64 + 2 * e], sl2, -m_eff));
-            const float p1 = ex2f(fmaf(x[64 + 2 * e + 1], sl2, -m_eff));
-            s0 += p0;
-            s1 += p1;
-            pb[e] = pack2(p0, p1);
+            const float2 y = tc::fma2(make_float2(x[64 + 2 * e], x[64 + 2 * e + 1]), sl2x2, nm2);
+            const float2 p = make_float2(ex2f(y.x), ex2f(y.y));
+            sum2 = tc::add2(sum2, p);
+            pb[e] = pack2(p.x, p.y);
         }
         tc::tmem_st32(tS + 32, pb);
-        l += s0 + s1;
+        l += sum2.x + sum2.y;
         tc::tmem_st_wait();
         tc::tc_fence_before();
         tc::mbar_arrive(tc::smem_addr(&bar[B_P + i]));
