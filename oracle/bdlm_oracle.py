@@ -127,12 +127,20 @@ def _docs(L, cu_seqlens):
 
 
 def _row_blocks(n, block):
-    """(first row, rows) of every query block of one sequence, clean then corrupted."""
+    """(first row, rows) of every query block of one sequence, clean then
+    corrupted. Blocks are cut from the start of each half, so when B does not
+    divide n the last block of each half holds n mod B rows."""
     out = []
     for half in (0, n):
-        for b in range(n // block):
-            out.append((half + b * block, block))
+        for r0 in range(0, n, block):
+            out.append((half + r0, min(block, n - r0)))
     return out
+
+
+def _block_rows(n, block, r0):
+    """Rows of the query block starting at doc-local row r0 (a block start)."""
+    base = 0 if r0 < n else n
+    return min(block, base + n - r0)
 
 
 def bdlm_attention(q, k, v, block, scale, cu_seqlens=None, do=None,
@@ -166,7 +174,7 @@ def bdlm_attention(q, k, v, block, scale, cu_seqlens=None, do=None,
     for di, r0 in work:
         s0, ln = docs[di]
         n = ln // 2
-        rows = np.arange(r0, r0 + block)
+        rows = np.arange(r0, r0 + _block_rows(n, block, r0))
         mrow = mask_rows(rows, n, block)
         cols = np.nonzero(mrow.any(axis=0))[0]
         sub = mrow[:, cols]
@@ -282,8 +290,11 @@ def group_attention(q_g, k_g, v_g, n, block, blocks, scale, do=None):
 
 
 def valid_pairs(n, block):
-    """Closed form of the mask's population per head for one sequence:
-    clean rows of block b see (b+1)B keys, corrupted rows of block b see bB
-    clean keys plus their own B corrupted keys, so each half contributes
-    B * sum_b (b+1) B = n (n + B) / 2, and the two halves n (n + B)."""
-    return n * (n + block)
+    """Closed form of the mask's population per head for one sequence.
+    With n = nb B + r: the clean rows of a full block b see (b+1)B keys, the
+    r rows of a last partial block see all n clean keys; the corrupted rows of
+    a full block b see bB clean keys plus their own B corrupted keys, those of
+    the partial block nb B + r = n. Each half contributes
+    B^2 nb (nb + 1) / 2 + r n; when B divides n this is n (n + B) for both."""
+    nb, r = divmod(n, block)
+    return block * block * nb * (nb + 1) + 2 * r * n
