@@ -52,7 +52,10 @@ def log(*a):
 
 
 def valid_pairs(n, block):
-    return n * (n + block)
+    """Valid (query, key) pairs per head of one sequence of clean length n:
+    n (n + B) when B divides n; with n = nb B + r, B^2 nb (nb + 1) + 2 r n."""
+    nb, r = divmod(n, block)
+    return block * block * nb * (nb + 1) + 2 * r * n
 
 
 def step_flops(w):

@@ -97,7 +97,7 @@ int check_common(const void* q, const void* k, const void* v, long long L, int b
     lay->L = L;
     if (cu) {
         if (kind != BDLM_PART_NONE) return BDLM_ERR_UNSUPPORTED;
-        if (n_docs <= 0 || (long long)n_docs * 2 * block > L) return BDLM_ERR_INVALID_ARG;
+        if (n_docs <= 0 || (long long)n_docs * 2 > L) return BDLM_ERR_INVALID_ARG;
         if (!aligned16(cu) && (reinterpret_cast<uintptr_t>(cu) & 3u)) return BDLM_ERR_INVALID_ARG;
         lay->mode = MODE_FULL;
         lay->cu = cu;
@@ -108,8 +108,7 @@ int check_common(const void* q, const void* k, const void* v, long long L, int b
         return BDLM_OK;
     }
     if (L % 2 != 0) return BDLM_ERR_INVALID_ARG;
-    const long long n = L / 2;
-    if (n % block != 0) return BDLM_ERR_INVALID_ARG;
+    const long long n = L / 2;  // any n: a last block may be short
     lay->n = (int)n;
     lay->n_docs = 1;
     cm->n = (int)n;
@@ -126,6 +125,8 @@ int check_common(const void* q, const void* k, const void* v, long long L, int b
         cm->Lq = L;
         cm->Lk = part->key_hi - part->key_lo;
     } else {
+        // a group's q rows are B per listed block, so its sequence has whole blocks
+        if (n % block != 0) return BDLM_ERR_INVALID_ARG;
         if (!part->q_blocks || part->n_q_blocks <= 0 || part->n_q_blocks > n / block) return BDLM_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(part->q_blocks) & 3u) return BDLM_ERR_INVALID_ARG;
         lay->mode = MODE_GROUP;

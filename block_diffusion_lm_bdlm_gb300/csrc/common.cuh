@@ -1,7 +1,9 @@
 // common.cuh - layout decode shared by the BDLM kernels.
 //
-// Every query row of a call has at most two key intervals, in k-row
-// coordinates of the call's k/v buffers:
+// Blocks are cut from the start of each half of a document; when B does not
+// divide the half's length n, the last block holds n mod B rows. Every query
+// row of a call has at most two key intervals, in k-row coordinates of the
+// call's k/v buffers:
 //   prefix [p_lo, p_hi): the clean keys it sees (clean blocks <= b for a clean
 //                        row of block b, clean blocks < b for a corrupted row),
 //   diag   [d_lo, d_hi): its own corrupted block (corrupted rows only).
@@ -209,7 +211,7 @@ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& 
         if ((b + 1) * B < n) { r.b_lo = n + (b + 1) * B; r.b_hi = 2 * n; }
     } else {
         r.a_lo = n + ((t.pos0 - n) / B) * B;
-        r.a_hi = n + ((t.pos0 + t.nrows - 1 - n) / B + 1) * B;
+        r.a_hi = imin(n + ((t.pos0 + t.nrows - 1 - n) / B + 1) * B, 2 * n);  // a last block may be short
     }
     return r;
 }
@@ -234,11 +236,11 @@ __device__ __forceinline__ KeyRows key_rows(const Layout& lay, const Tile& t, in
         const int bk = kc / B;
         r.a_lo = bk * B;
         r.a_hi = n;
-        r.b_lo = n + (bk + 1) * B;
+        r.b_lo = n + (bk + 1) * B;  // empty when the key's block is the last
         r.b_hi = 2 * n;
     } else {
         r.a_lo = n + ((kc - n) / B) * B;
-        r.a_hi = r.a_lo + B;
+        r.a_hi = imin(r.a_lo + B, 2 * n);  // a last block may be short
     }
     return r;
 }

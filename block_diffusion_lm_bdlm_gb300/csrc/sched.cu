@@ -98,7 +98,7 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         for (int d = tid; d < ndocs; d += kThreads) {
             long long s = __ldg(lay.cu + d), e = __ldg(lay.cu + d + 1);
             long long len = e - s;
-            if (len <= 0 || (len & 1) || ((len / 2) % lay.B) != 0) { bad = 1; bad_info = d; }
+            if (len <= 0 || (len & 1)) { bad = 1; bad_info = d; }  // [clean | corrupted] halves
         }
         if (tid == 0 && (__ldg(lay.cu) != 0 || (long long)__ldg(lay.cu + ndocs) != lay.L)) {
             bad = 1;

@@ -19,7 +19,9 @@
  *       lse          : fp32 [H, Lq]          (natural log of sum_j exp(scale*q.k_j))
  *   - Query head h reads kv head h / (H / Hk).
  *   - d is 64 or 128; H % Hk == 0; 1 <= B <= 1024; every document's clean
- *     length is a positive multiple of B.
+ *     length n is positive. Blocks are cut from the start of each half, so
+ *     when B does not divide n the last block of each half holds n mod B rows
+ *     (a BLOCK_GROUP call needs whole blocks: B must divide n).
  *   - The caller owns every buffer, including the workspace. The library never
  *     allocates or frees device memory and never synchronises, except in
  *     bdlm_read_error. Every call is asynchronous on `stream` (NULL = the

@@ -83,7 +83,8 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, q=None) == INVALID
     assert _fwd(lib, k=17) == INVALID            # misaligned
     assert _fwd(lib, L=255) == INVALID           # odd total length
-    assert _fwd(lib, L=200) == INVALID           # n = 100 not a multiple of 16
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 1, 0, 0, 16)
+    assert _fwd(lib, L=200, part=ctypes.byref(p)) == INVALID  # a group needs whole blocks (n = 100, B = 16)
     assert _fwd(lib, heads=3, kv_heads=2) == INVALID
     assert _fwd(lib, head_dim=96) == UNSUP
     assert _fwd(lib, ws=None) == WS

@@ -306,6 +306,82 @@ def test_packed_documents(bd):
     check_grad(host(dv), r["dv"], "dv")
 
 
+# ragged last blocks: B does not divide the clean length
+RAGGED = [
+    # n, block, H, Hk, d
+    (100, 16, 2, 1, 128),   # 6 whole blocks + 4 rows
+    (70, 32, 4, 2, 64),     # warp-level backward
+    (45, 8, 3, 3, 128),
+    (37, 64, 2, 2, 128),    # B > n: one short block per half
+    (129, 128, 2, 1, 128),  # one whole block and one row
+    (300, 64, 4, 1, 128),   # several 128-row tiles, short last block
+]
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d", RAGGED)
+def test_ragged_last_block(bd, n, block, H, Hk, d):
+    w, x = gen(n, block, H, Hk, d, seed=7 * n + block)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block)
+    torch.cuda.synchronize()
+    r = ref_full(x, w)
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
+
+
+def test_ragged_packed_documents(bd):
+    block, H, Hk, d = 16, 4, 2, 128
+    lens = [2 * 37, 2 * 100, 2 * 5, 2 * 129, 2 * 64, 2 * 1]
+    cu = synth.cu_seqlens_of(lens)
+    g = torch.Generator(device="cuda").manual_seed(17)
+    T = cu[-1]
+    mk = lambda *s: (torch.randn(*s, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    q, k, v = mk(T, H, d), mk(T, Hk, d), mk(T, Hk, d)
+    do = (torch.randn(T, H, d, device="cuda", generator=g)).to(torch.bfloat16)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o, lse = bd.bdlm_attn_fwd(q, k, v, block, cu_seqlens=cu_d)
+    dq, dk, dv = bd.bdlm_attn_bwd(q, k, v, o, lse, do, block, cu_seqlens=cu_d)
+    torch.cuda.synchronize()
+    r = oracle.bdlm_attention(host(q), host(k), host(v), block, 1 / math.sqrt(d), cu_seqlens=cu, do=host(do))
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
+
+
+def test_ragged_sharded_forward_merge_backward(bd):
+    n, block, H, Hk, d = 100, 16, 4, 2, 128
+    w, x = gen(n, block, H, Hk, d, seed=19)
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, do=do64)
+    windows = synth.shard_bounds(n, 3) + [(n, 2 * n)]
+    parts, lses = [], []
+    for lo, hi in windows:
+        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), block,
+                                  part=bd.Partial.window(lo, hi))
+        parts.append(po)
+        lses.append(pl)
+    o, lse = bd.bdlm_lse_merge(parts, lses)
+    dq_sum = torch.zeros(x.q.shape, dtype=torch.float32, device="cuda")
+    dk, dv = torch.empty_like(x.k), torch.empty_like(x.v)
+    for lo, hi in windows:
+        sq, sk, sv = bd.bdlm_attn_bwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), o, lse, x.do, block,
+                                      part=bd.Partial.window(lo, hi))
+        dq_sum += sq.float()
+        dk[lo:hi] = sk
+        dv[lo:hi] = sv
+    torch.cuda.synchronize()
+    check_o(host(o), full["o"], "merged o")
+    check_lse(host(lse), full["lse"], "merged lse")
+    check_grad(host(dq_sum), full["dq"], "sum of dq shares")
+    check_grad(host(dk), full["dk"], "dk")
+    check_grad(host(dv), full["dv"], "dv")
+
+
 def test_zero_keys_closed_form(bd):
     n, block, H, d = 192, 16, 2, 128
     w, x = gen(n, block, H, H, d, seed=17)
@@ -328,13 +404,15 @@ def test_malformed_cu_seqlens_is_reported(bd):
     T = 256
     q = torch.zeros(T, H, d, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(T, H, d, 2), dtype=torch.uint8, device="cuda")
-    for bad in ([0, 63, 256], [0, 96, 256], [0, 128, 200]):
+    # odd document length, an empty document, decreasing offsets, wrong total
+    for bad in ([0, 63, 256], [0, 0, 256], [0, 200, 128], [0, 128, 200]):
         cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
         bd.bdlm_attn_fwd(q, q, q, block, cu_seqlens=cu, workspace=ws)
         assert bd.bdlm_read_error(ws) == 6, bad
-    cu = torch.tensor([0, 128, 256], dtype=torch.int32, device="cuda")
-    bd.bdlm_attn_fwd(q, q, q, block, cu_seqlens=cu, workspace=ws)
-    assert bd.bdlm_read_error(ws) == 0
+    for good in ([0, 128, 256], [0, 96, 256]):  # the second has short last blocks (48 and 80 clean rows, B = 32)
+        cu = torch.tensor(good, dtype=torch.int32, device="cuda")
+        bd.bdlm_attn_fwd(q, q, q, block, cu_seqlens=cu, workspace=ws)
+        assert bd.bdlm_read_error(ws) == 0, good
 
 
 def test_forward_is_deterministic(bd):
