@@ -213,17 +213,18 @@ def dense_bdlm_attention(q, k, v, n, block, scale, do=None):
 # parallelism (Block Parallelism abstract; rit.work post, CSBP paragraph).
 # ----------------------------------------------------------------------------
 def partial_attention(q, k_win, v_win, n, block, key_lo, key_hi, scale, do=None, o_full=None,
-                      lse_full=None):
-    """q holds all 2n rows of one sequence; k_win/v_win hold the keys at
-    positions [key_lo, key_hi) only. Rows with no visible key in the window
-    get o = 0, lse = -inf.
+                      lse_full=None, q_lo=0, q_hi=None):
+    """q holds the rows at positions [q_lo, q_hi) of one sequence (default all
+    2n); k_win/v_win hold the keys at positions [key_lo, key_hi) only. Rows
+    with no visible key in the window get o = 0, lse = -inf.
 
     With `do`, also returns the window's share of the gradients taken with the
-    FULL attention's softmax (o_full, lse_full): dq from these keys only, and
-    dk, dv of the window's keys. Summed over a partition of the keys these give
-    the unsharded gradients.
+    FULL attention's softmax (o_full, lse_full, for the same rows): dq from
+    these keys only, and dk, dv of the window's keys from these rows only.
+    Summed over a partition of the keys (and, for dk and dv, of the rows)
+    these give the unsharded gradients.
     """
-    rows = np.arange(2 * n)
+    rows = np.arange(q_lo, 2 * n if q_hi is None else q_hi)
     cols = np.arange(key_lo, key_hi)
     m = mask_rows(rows, n, block, cols)
     o, lse = attend(q, k_win, v_win, m, scale)

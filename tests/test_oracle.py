@@ -258,6 +258,39 @@ def test_shard_then_merge_equals_unsharded(shards):
     np.testing.assert_allclose(dv, full["dv"], atol=1e-12)
 
 
+@pytest.mark.parametrize("n,block", [(48, 8), (45, 8)])
+def test_row_range_by_key_window_grid(n, block):
+    # Token-level tasks: any partition of the query rows by any partition of
+    # the keys; per row range, merging its key windows gives the unsharded
+    # attention rows and dq; dk, dv summed over every task give the unsharded
+    # key gradients.
+    H, Hk, d = 4, 2, 8
+    q, k, v, do = case(n, block, H, Hk, d, seed=62)
+    scale = 0.3
+    full = oracle.dense_bdlm_attention(q, k, v, n, block, scale, do=do)
+    row_cuts = [0, 7, n - 3, n, n + 13, 2 * n]
+    key_cuts = [0, 11, n - 5, n, n + 20, 2 * n]
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for qa, qb in zip(row_cuts[:-1], row_cuts[1:]):
+        os_, ls_ = [], []
+        dq = np.zeros((qb - qa,) + q.shape[1:])
+        for ka, kb in zip(key_cuts[:-1], key_cuts[1:]):
+            p = oracle.partial_attention(q[qa:qb], k[ka:kb], v[ka:kb], n, block, ka, kb, scale, do=do[qa:qb],
+                                         o_full=full["o"][qa:qb], lse_full=full["lse"][:, qa:qb], q_lo=qa, q_hi=qb)
+            os_.append(p["o"])
+            ls_.append(p["lse"])
+            dq += p["dq"]
+            dk[ka:kb] += p["dk"]
+            dv[ka:kb] += p["dv"]
+        o, lse = oracle.lse_merge(os_, ls_)
+        np.testing.assert_allclose(o, full["o"][qa:qb], atol=1e-12)
+        np.testing.assert_allclose(lse, full["lse"][:, qa:qb], atol=1e-12)
+        np.testing.assert_allclose(dq, full["dq"][qa:qb], atol=1e-12)
+    np.testing.assert_allclose(dk, full["dk"], atol=1e-12)
+    np.testing.assert_allclose(dv, full["dv"], atol=1e-12)
+
+
 def test_merge_special_cases():
     rng = np.random.default_rng(70)
     R, H, d = 5, 2, 3
