@@ -48,7 +48,7 @@ class BDLMError(RuntimeError):
 class _CPartial(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("n_q_blocks", ctypes.c_int32), ("key_lo", ctypes.c_int64),
                 ("key_hi", ctypes.c_int64), ("q_blocks", ctypes.c_void_p), ("flags", ctypes.c_int32),
-                ("o_dtype", ctypes.c_int32)]
+                ("o_dtype", ctypes.c_int32), ("q_lo", ctypes.c_int64), ("q_hi", ctypes.c_int64)]
 
 
 @dataclass
@@ -58,6 +58,8 @@ class Partial:
     Partial.window(lo, hi): k/v hold the keys at positions [lo, hi).
     Partial.window(lo, hi, accumulate=True): forward only; `out` and `lse`
         hold the merged result of earlier windows and this call merges in.
+    Partial.window(lo, hi, q_lo=a, q_hi=b): q (o, lse, dO, dq) hold only the
+        rows at positions [a, b); pass L = 2n to the call.
     Partial.group(blocks): q holds the corrupted rows of `blocks` (device int32).
     The element type of a partial forward's o follows the `out` tensor (bf16
     or fp32).
@@ -67,10 +69,17 @@ class Partial:
     key_hi: int = 0
     q_blocks: Optional[torch.Tensor] = None
     accumulate: bool = False
+    q_lo: int = 0
+    q_hi: int = 0
 
     @staticmethod
-    def window(lo: int, hi: int, accumulate: bool = False) -> "Partial":
-        return Partial(PART_KEY_WINDOW, key_lo=int(lo), key_hi=int(hi), accumulate=bool(accumulate))
+    def window(lo: int, hi: int, accumulate: bool = False, q_lo: int = 0, q_hi: int = 0) -> "Partial":
+        return Partial(PART_KEY_WINDOW, key_lo=int(lo), key_hi=int(hi), accumulate=bool(accumulate),
+                       q_lo=int(q_lo), q_hi=int(q_hi))
+
+    @property
+    def row_range(self) -> bool:
+        return self.q_hi != 0 or self.q_lo != 0
 
     @staticmethod
     def group(blocks: torch.Tensor) -> "Partial":
@@ -84,7 +93,7 @@ class Partial:
                 raise ValueError("q_blocks must be a contiguous int32 CUDA tensor")
             nb, ptr = b.numel(), b.data_ptr()
         flags = PART_ACCUMULATE if self.accumulate else 0
-        return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr, flags, o_dtype)
+        return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr, flags, o_dtype, self.q_lo, self.q_hi)
 
 
 _lib = None
@@ -164,6 +173,16 @@ def bdlm_last_launch_count() -> int:
     return int(load_library().bdlm_last_launch_count())
 
 
+def _total_rows(q, L, part):
+    """L of the call: q's rows by default; a block group or a window over a
+    row range must name the sequence's 2n."""
+    if L is not None:
+        return int(L)
+    if part is not None and (part.kind == PART_BLOCK_GROUP or part.row_range):
+        raise ValueError("pass L = 2n: q holds only some rows of the sequence")
+    return q.shape[0]
+
+
 def _fwd_outputs(q, part, out, lse):
     """Allocate or check the forward's o and lse; returns (out, lse, o_dtype)."""
     Lq, H, d = q.shape
@@ -194,7 +213,7 @@ def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=No
         _bf16_cuda(nm, t)
     Lq, H, d = q.shape
     Hk = k.shape[1]
-    L = Lq if L is None else int(L)
+    L = _total_rows(q, L, part)
     cu_ptr, n_docs = _cu(cu_seqlens)
     out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
     ws_bytes = lib.bdlm_attn_fwd_workspace_bytes(L, H, d, n_docs)
@@ -220,7 +239,7 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
         _bf16_cuda(nm, t)
     Lq, H, d = q.shape
     Hk = k.shape[1]
-    L = Lq if L is None else int(L)
+    L = _total_rows(q, L, part)
     cu_ptr, n_docs = _cu(cu_seqlens)
     out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
     cpart = ctypes.byref(part.c(o_dtype)) if part is not None else None
@@ -242,7 +261,7 @@ def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, L: Optional[int] = None, c
         _bf16_cuda(nm, t)
     Lq, H, d = q.shape
     Hk = k.shape[1]
-    L = Lq if L is None else int(L)
+    L = _total_rows(q, L, part)
     cu_ptr, n_docs = _cu(cu_seqlens)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk

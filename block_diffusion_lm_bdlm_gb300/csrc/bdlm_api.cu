@@ -118,13 +118,18 @@ int check_common(const void* q, const void* k, const void* v, long long L, int b
         cm->Lq = cm->Lk = L;
     } else if (kind == BDLM_PART_KEY_WINDOW) {
         if (part->key_lo < 0 || part->key_hi <= part->key_lo || part->key_hi > L) return BDLM_ERR_INVALID_ARG;
+        const bool all_rows = part->q_lo == 0 && part->q_hi == 0;
+        if (!all_rows && (part->q_lo < 0 || part->q_hi <= part->q_lo || part->q_hi > L)) return BDLM_ERR_INVALID_ARG;
         lay->mode = MODE_WINDOW;
         lay->kw_lo = (int)part->key_lo;
         lay->kw_hi = (int)part->key_hi;
+        lay->q_lo = all_rows ? 0 : (int)part->q_lo;
+        lay->q_hi = all_rows ? (int)L : (int)part->q_hi;
         cm->mode = MODE_WINDOW;
-        cm->Lq = L;
+        cm->Lq = lay->q_hi - lay->q_lo;
         cm->Lk = part->key_hi - part->key_lo;
     } else {
+        if (part->q_lo != 0 || part->q_hi != 0) return BDLM_ERR_INVALID_ARG;  // row ranges are for windows
         // a group's q rows are B per listed block, so its sequence has whole blocks
         if (n % block != 0) return BDLM_ERR_INVALID_ARG;
         if (!part->q_blocks || part->n_q_blocks <= 0 || part->n_q_blocks > n / block) return BDLM_ERR_INVALID_ARG;

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
             const int p0 = rem < na ? ra_lo + rem * BQ : rb_lo + (rem - na) * BQ;
             const int hi = rem < na ? ra_hi : rb_hi;
             const Tile qt{kt.doc_start, n, p0, imin(BQ, hi - p0)};
-            const long long qr0 = (long long)kt.doc_start + p0;
+            const long long qr0 = q_row_of(a.lay, kt, p0);
             load_tile_async<D, BQ, NT>(sQ0 + buf * BQ * D * 2, a.q, qr0, qr0 + qt.nrows, q_stride, h);
             load_tile_async<D, BQ, NT>(sO0 + buf * BQ * D * 2, a.dO, qr0, qr0 + qt.nrows, q_stride, h);
             cp_async_commit();
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
             const int h = kvh * G + hh;
             const int p0 = rem < na ? ra_lo + rem * BQ : rb_lo + (rem - na) * BQ;
             const int qrows = imin(BQ, (rem < na ? ra_hi : rb_hi) - p0);
-            const long long qr0 = (long long)kt.doc_start + p0;
+            const long long qr0 = q_row_of(a.lay, kt, p0);
             const uint32_t sQ = sQ0 + buf * BQ * D * 2, sO = sO0 + buf * BQ * D * 2;
 
             // S^T and dP^T for this warp's 16 keys x 64 query rows

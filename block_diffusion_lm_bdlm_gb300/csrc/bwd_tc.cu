@@ -175,7 +175,7 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
         if (!__all_sync(0xffffffffu, got)) return;
         int h, p0, nrows;
         step_rows(c, a, s, &h, &p0, &nrows);
-        const int qr0 = c.kt.doc_start + p0;
+        const int qr0 = q_row_of(a.lay, c.kt, p0);
         const uint32_t bf = tc::smem_addr(&bar[B_QDF + st]);
         if (lane == 0) {
             mbar_expect_tx(bf, 2 * kQT);
@@ -417,7 +417,7 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
             tc::fence_proxy_async_smem();
             named_sync(2, 128);
             if (leader) {
-                tma_reduce_add_3d(tdq, sbase + SM_STG + half * kStg, 0, h, c.kt.doc_start + p0 + kHalfRows * half);
+                tma_reduce_add_3d(tdq, sbase + SM_STG + half * kStg, 0, h, q_row_of(a.lay, c.kt, p0) + kHalfRows * half);
                 bulk_commit();
                 if (half == 1) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));
             }

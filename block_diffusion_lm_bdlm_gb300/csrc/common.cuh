@@ -41,6 +41,7 @@ struct Layout {
     int B;             // diffusion block size
     int n;             // clean length (single sequence / window / group)
     int kw_lo, kw_hi;  // MODE_WINDOW: key positions held by k/v
+    int q_lo, q_hi;    // MODE_WINDOW: query positions held by q (q row = position - q_lo)
     const int* cu;     // MODE_FULL: device cu_seqlens, or nullptr for one sequence
     int n_docs;
     long long L;       // rows of the full concatenation
@@ -128,8 +129,12 @@ __device__ __forceinline__ TileRange tile_range(const Layout& lay, const Tile& t
             g.r2_lo = imin(g.r2_lo, s.d_lo);
             g.r2_hi = imax(g.r2_hi, s.d_hi);
         }
+        // first row of the next block; blocks are cut from the start of each
+        // half (a group's list rows from 0), which is not a multiple of B when
+        // B does not divide n
         const int pos = t.pos0 + r;
-        const int nxt = (pos / B + 1) * B - t.pos0;  // first row of the next block
+        const int half0 = (lay.mode == MODE_GROUP || pos < t.n) ? 0 : t.n;
+        const int nxt = half0 + ((pos - half0) / B + 1) * B - t.pos0;
         r = nxt > r ? nxt : r + 1;
     }
     if (g.r1_hi == 0) g.r1_lo = 0;
@@ -178,6 +183,12 @@ __device__ __forceinline__ int group_count_le(const Layout& lay, int b) {
     return lo;
 }
 
+// q row of row position p of a tile (full: document start + position;
+// window: position - q_lo; group: the list row itself).
+__device__ __forceinline__ int q_row_of(const Layout& lay, const Tile& t, int p) {
+    return t.doc_start + p - (lay.mode == MODE_WINDOW ? lay.q_lo : 0);
+}
+
 // k row of key 0 of backward tile t.
 __device__ __forceinline__ int key_row0(const Layout& lay, const Tile& t) {
     return lay.mode == MODE_WINDOW ? t.pos0 - lay.kw_lo : t.doc_start + t.pos0;
@@ -212,6 +223,14 @@ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& 
     } else {
         r.a_lo = n + ((t.pos0 - n) / B) * B;
         r.a_hi = imin(n + ((t.pos0 + t.nrows - 1 - n) / B + 1) * B, 2 * n);  // a last block may be short
+    }
+    if (lay.mode == MODE_WINDOW) {  // only the call's query rows
+        r.a_lo = imax(r.a_lo, lay.q_lo);
+        r.a_hi = imin(r.a_hi, lay.q_hi);
+        if (r.a_hi <= r.a_lo) { r.a_lo = 0; r.a_hi = 0; }
+        r.b_lo = imax(r.b_lo, lay.q_lo);
+        r.b_hi = imin(r.b_hi, lay.q_hi);
+        if (r.b_hi <= r.b_lo) { r.b_lo = 0; r.b_hi = 0; }
     }
     return r;
 }

@@ -361,7 +361,7 @@ __device__ __forceinline__ ItemCtx decode(const FwdArgs& a, const TileRange* ran
     c.two = 2 * hp + 1 < a.G;
     c.n1 = (c.R.r1_hi - c.R.r1_lo + BN - 1) / BN;
     c.nk = c.n1 + (c.R.r2_hi - c.R.r2_lo + BN - 1) / BN;
-    c.q_row0 = c.T.doc_start + c.T.pos0;
+    c.q_row0 = q_row_of(a.lay, c.T, c.T.pos0);
     return c;
 }
 

@@ -120,16 +120,17 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     }
 
     // ---- enumeration ---------------------------------------------------------
-    if (kind == 1 && lay.mode != MODE_FULL) {
-        // key tiles over the call's keys, in two runs that never straddle the
-        // clean/corrupted boundary: sequence positions of the window, or the
-        // group's k rows (clean [0, n), then its corrupted rows)
+    if (lay.mode == MODE_WINDOW || (kind == 1 && lay.mode == MODE_GROUP)) {
+        // tiles in two runs that never straddle the clean/corrupted boundary:
+        // forward - the window's query positions; backward - the window's key
+        // positions, or the group's k rows (clean [0, n), then its corrupted rows)
         int c_lo, c_hi, x_lo, x_hi;
         if (lay.mode == MODE_WINDOW) {
-            c_lo = lay.kw_lo;
-            c_hi = imin(lay.kw_hi, lay.n);
-            x_lo = imax(lay.kw_lo, lay.n);
-            x_hi = lay.kw_hi;
+            const int lo = kind == 0 ? lay.q_lo : lay.kw_lo, hi = kind == 0 ? lay.q_hi : lay.kw_hi;
+            c_lo = lo;
+            c_hi = imin(hi, lay.n);
+            x_lo = imax(lo, lay.n);
+            x_hi = hi;
         } else {
             c_lo = 0;
             c_hi = lay.n;

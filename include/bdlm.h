@@ -102,6 +102,12 @@ enum bdlm_part_flags {
  *   the window's result (their o is not read). The first window of a sequence
  *   is an ordinary call without the flag. This replaces storing every window's
  *   partial and one bdlm_lse_merge call.
+ * q_lo, q_hi (KEY_WINDOW only): a token-level task (Core Attention
+ *   Disaggregation abstract: attention over token-level shards). q, o, lse
+ *   (and for the backward dO, dq) hold only the rows at sequence positions
+ *   [q_lo, q_hi), Lq = q_hi - q_lo, e.g. one rank's own rows against one
+ *   gathered clean shard; q_hi = 0 selects all L rows. The backward's dk, dv
+ *   are then the window keys' gradients from these rows only.
  * o_dtype: BDLM_BF16 (0, default) or BDLM_F32 - the element type of o for a
  *   KEY_WINDOW or BLOCK_GROUP forward (fp32 keeps a running merge from being
  *   rounded at every window). Full attention and the backward take bf16 o.
@@ -113,6 +119,7 @@ typedef struct {
     const int32_t* q_blocks; /* BLOCK_GROUP: device int32 [n_q_blocks]            */
     int32_t flags;           /* enum bdlm_part_flags (0 = none)                   */
     int32_t o_dtype;         /* enum bdlm_dtype of o (forward partials)           */
+    int64_t q_lo, q_hi;      /* KEY_WINDOW: q holds positions [q_lo, q_hi); 0,0 = all L rows */
 } bdlm_partial;
 
 /* Workspace sizes (bytes) for one call with L query rows, H heads, head dim d

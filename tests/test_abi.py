@@ -106,6 +106,12 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # unknown o dtype
     p = bd._CPartial(bd.PART_NONE, 0, 0, 0, None, 0, bd.BDLM_F32)
     assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # fp32 o is for partials
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, 0, 0, 10, 5)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # empty row range
+    p = bd._CPartial(bd.PART_KEY_WINDOW, 0, 0, 64, None, 0, 0, 0, 300)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # rows past the sequence
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 1, 0, 0, 16, 0, 0, 0, 16)
+    assert _fwd(lib, part=ctypes.byref(p)) == INVALID   # row ranges are for windows
     assert lib.bdlm_last_launch_count() == 0
 
 

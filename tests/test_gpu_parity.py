@@ -306,6 +306,40 @@ def test_packed_documents(bd):
     check_grad(host(dv), r["dv"], "dv")
 
 
+# token-level tasks: (query row range) x (key window) over one sequence
+@pytest.mark.parametrize("n,block,H,Hk,d", [(100, 16, 4, 2, 128), (90, 8, 2, 2, 64)])
+def test_row_range_by_key_window_tasks(bd, n, block, H, Hk, d):
+    w, x = gen(n, block, H, Hk, d, seed=23 + n)
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, do=do64)
+    o_g, lse_g = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)  # the backward's softmax statistics
+    row_cuts = [0, 7, n - 3, n, n + 13, 2 * n]
+    key_cuts = [0, 11, n - 5, n, n + 20, 2 * n]
+    L = 2 * n
+    dk = torch.zeros(x.k.shape, dtype=torch.float32, device="cuda")
+    dv = torch.zeros(x.v.shape, dtype=torch.float32, device="cuda")
+    for qa, qb in zip(row_cuts[:-1], row_cuts[1:]):
+        qr, dor = x.q[qa:qb].contiguous(), x.do[qa:qb].contiguous()
+        o = torch.empty(qr.shape, dtype=torch.float32, device="cuda")
+        lse = torch.empty((H, qb - qa), dtype=torch.float32, device="cuda")
+        dq = torch.zeros(qr.shape, dtype=torch.float32, device="cuda")
+        for i, (ka, kb) in enumerate(zip(key_cuts[:-1], key_cuts[1:])):
+            kw, vw = x.k[ka:kb].contiguous(), x.v[ka:kb].contiguous()
+            bd.bdlm_attn_fwd(qr, kw, vw, block, L=L, out=o, lse=lse,
+                             part=bd.Partial.window(ka, kb, accumulate=i > 0, q_lo=qa, q_hi=qb))
+            sq, sk, sv = bd.bdlm_attn_bwd(qr, kw, vw, o_g[qa:qb].contiguous(), lse_g[:, qa:qb].contiguous(), dor,
+                                          block, L=L, part=bd.Partial.window(ka, kb, q_lo=qa, q_hi=qb))
+            dq += sq.float()
+            dk[ka:kb] += sk.float()
+            dv[ka:kb] += sv.float()
+        torch.cuda.synchronize()
+        check_o(host(o), full["o"][qa:qb], f"rows [{qa},{qb}) o")
+        check_lse(host(lse), full["lse"][:, qa:qb], f"rows [{qa},{qb}) lse")
+        check_grad(host(dq), full["dq"][qa:qb], f"rows [{qa},{qb}) dq")
+    check_grad(host(dk), full["dk"], "dk over all tasks")
+    check_grad(host(dv), full["dv"], "dv over all tasks")
+
+
 # ragged last blocks: B does not divide the clean length
 RAGGED = [
     # n, block, H, Hk, d
