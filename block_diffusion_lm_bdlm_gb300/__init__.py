@@ -24,7 +24,7 @@ from .build import LIB
 __all__ = [
     "BDLMError", "Partial", "bdlm_attn_fwd", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_last_launch_count",
-    "load_library", "EXPORTED_SYMBOLS",
+    "bdlm_selftest_timeout", "load_library", "EXPORTED_SYMBOLS",
 ]
 
 BDLM_OK = 0
@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_attn_fwd", "bdlm_attn_bwd",
     "bdlm_lse_merge", "bdlm_read_error", "bdlm_status_string", "bdlm_last_launch_count",
     "bdlm_attn_fwd_noalloc",
+    "bdlm_selftest_timeout",
 )
 
 
@@ -129,6 +130,8 @@ def load_library() -> ctypes.CDLL:
     lib.bdlm_status_string.restype = ctypes.c_char_p
     lib.bdlm_last_launch_count.argtypes = []
     lib.bdlm_last_launch_count.restype = ctypes.c_int
+    lib.bdlm_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
+    lib.bdlm_selftest_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -303,6 +306,14 @@ def bdlm_lse_merge(partials: Sequence[torch.Tensor], lses: Sequence[torch.Tensor
                             out.data_ptr(), lse.data_ptr(), _stream(stream))
     _check(st, "bdlm_lse_merge")
     return out, lse
+
+
+def bdlm_selftest_timeout(workspace: torch.Tensor, wait_ns: int = 100_000_000, stream=None) -> None:
+    """Run the device failure-path self-test: a wait that nothing completes
+    gives up after wait_ns and records BDLM_ERR_TIMEOUT in `workspace` (read it
+    with bdlm_read_error)."""
+    st = load_library().bdlm_selftest_timeout(workspace.data_ptr(), workspace.numel(), int(wait_ns), _stream(stream))
+    _check(st, "bdlm_selftest_timeout")
 
 
 def bdlm_read_error(workspace: torch.Tensor, stream=None) -> int:

@@ -243,6 +243,19 @@ BDLM_API const char* bdlm_status_string(int status);
  * launched (for launch accounting in benchmarks). */
 BDLM_API int bdlm_last_launch_count(void);
 
+/*
+ * Self-test of the device failure path: launches one CTA that waits, with the
+ * same bounded mbarrier wait every tensor-core kernel uses, for a barrier
+ * phase that nothing completes. The wait gives up after wait_ns (clamped to
+ * [1 ms, 2 s]), writes BDLM_ERR_TIMEOUT to the workspace error word and the
+ * kernel returns; nothing faults and the context stays usable. The workspace
+ * needs 256 bytes (its header); bdlm_read_error then returns
+ * BDLM_ERR_TIMEOUT. Returns BDLM_ERR_WORKSPACE for a missing or small
+ * workspace.
+ */
+BDLM_API int bdlm_selftest_timeout(void* workspace, size_t workspace_bytes, uint32_t wait_ns,
+                  bdlm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -115,6 +115,12 @@ def test_forward_rejects_bad_arguments(lib):
     assert lib.bdlm_last_launch_count() == 0
 
 
+def test_selftest_rejects_a_missing_workspace(lib):
+    assert lib.bdlm_selftest_timeout(None, 256, 1000000, None) == 3   # BDLM_ERR_WORKSPACE
+    assert lib.bdlm_selftest_timeout(256, 16, 1000000, None) == 3     # smaller than the header
+    assert lib.bdlm_selftest_timeout(272, 256, 1000000, None) == 3    # not 256-byte aligned
+
+
 def test_backward_and_merge_reject_bad_arguments(lib):
     import block_diffusion_lm_bdlm_gb300 as bd
 
