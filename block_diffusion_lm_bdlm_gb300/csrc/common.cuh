@@ -74,15 +74,25 @@ struct TileRange {
 __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 
+// Read-only load (through the read-only cache on the device). The layout
+// helpers below also compile for the host, where the tests check them.
+__host__ __device__ __forceinline__ int ld_ro(const int* p) {
+#ifdef __CUDA_ARCH__
+    return __ldg(p);
+#else
+    return *p;
+#endif
+}
+
 // Key intervals of tile row r (empty intervals are [0, 0)).
-__device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r) {
+__host__ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r) {
     Span s{0, 0, 0, 0};
     if (r >= t.nrows) return s;
     const int B = lay.B;
     if (lay.mode == MODE_GROUP) {
         const int j = t.pos0 + r;
         const int li = j / B;
-        const int b = __ldg(lay.blocks + li);
+        const int b = ld_ro(lay.blocks + li);
         if (b > 0) { s.p_lo = 0; s.p_hi = b * B; }
         s.d_lo = lay.n + li * B;
         s.d_hi = s.d_lo + B;
@@ -112,7 +122,7 @@ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r
 
 // Exact key ranges of tile t: one span per diffusion block of rows (all rows
 // of a block share one span).
-__device__ __forceinline__ TileRange tile_range(const Layout& lay, const Tile& t) {
+__host__ __device__ __forceinline__ TileRange tile_range(const Layout& lay, const Tile& t) {
     TileRange g{0x7fffffff, 0, 0x7fffffff, 0, 0, 0x7fffffff, 0, 0};
     const int B = lay.B;
     for (int r = 0; r < t.nrows;) {
@@ -143,7 +153,7 @@ __device__ __forceinline__ TileRange tile_range(const Layout& lay, const Tile& t
     return g;
 }
 
-__device__ __forceinline__ bool span_sees(const Span& s, int kr) {
+__host__ __device__ __forceinline__ bool span_sees(const Span& s, int kr) {
     return (kr >= s.p_lo && kr < s.p_hi) || (kr >= s.d_lo && kr < s.d_hi);
 }
 
@@ -156,11 +166,11 @@ struct RelInterval {
     int lo;
     unsigned len;
 };
-__device__ __forceinline__ RelInterval range_interval(const Span& s, bool prefix, int k0) {
+__host__ __device__ __forceinline__ RelInterval range_interval(const Span& s, bool prefix, int k0) {
     const int lo = prefix ? s.p_lo : s.d_lo, hi = prefix ? s.p_hi : s.d_hi;
     return RelInterval{lo - k0, (unsigned)(hi > lo ? hi - lo : 0)};
 }
-__device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) { return (unsigned)(e - r.lo) < r.len; }
+__host__ __device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) { return (unsigned)(e - r.lo) < r.len; }
 
 // ---------------------------------------------------------------------------
 // Key-major view (backward). A backward tile is a run of consecutive keys that
@@ -174,23 +184,23 @@ __device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) { return (
 // Number of list entries with block id <= b. The backward requires a strictly
 // ascending block list, so the group rows that see a clean key of block b are
 // the list rows from group_count_le(b) * B on.
-__device__ __forceinline__ int group_count_le(const Layout& lay, int b) {
+__host__ __device__ __forceinline__ int group_count_le(const Layout& lay, int b) {
     int lo = 0, hi = lay.n_blocks;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(lay.blocks + mid) <= b) lo = mid + 1; else hi = mid;
+        if (ld_ro(lay.blocks + mid) <= b) lo = mid + 1; else hi = mid;
     }
     return lo;
 }
 
 // q row of row position p of a tile (full: document start + position;
 // window: position - q_lo; group: the list row itself).
-__device__ __forceinline__ int q_row_of(const Layout& lay, const Tile& t, int p) {
+__host__ __device__ __forceinline__ int q_row_of(const Layout& lay, const Tile& t, int p) {
     return t.doc_start + p - (lay.mode == MODE_WINDOW ? lay.q_lo : 0);
 }
 
 // k row of key 0 of backward tile t.
-__device__ __forceinline__ int key_row0(const Layout& lay, const Tile& t) {
+__host__ __device__ __forceinline__ int key_row0(const Layout& lay, const Tile& t) {
     return lay.mode == MODE_WINDOW ? t.pos0 - lay.kw_lo : t.doc_start + t.pos0;
 }
 
@@ -201,7 +211,7 @@ __device__ __forceinline__ int key_row0(const Layout& lay, const Tile& t) {
 struct KeyRows {
     int a_lo, a_hi, b_lo, b_hi;
 };
-__device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& t) {
+__host__ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& t) {
     KeyRows r{0, 0, 0, 0};
     const int n = t.n, B = lay.B;
     if (lay.mode == MODE_GROUP) {
@@ -237,7 +247,7 @@ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& 
 
 // The same for key kk of tile t alone (one interval per range; all empty for
 // kk >= t.nrows).
-__device__ __forceinline__ KeyRows key_rows(const Layout& lay, const Tile& t, int kk) {
+__host__ __device__ __forceinline__ KeyRows key_rows(const Layout& lay, const Tile& t, int kk) {
     KeyRows r{0, 0, 0, 0};
     if (kk >= t.nrows) return r;
     const int n = t.n, B = lay.B, kc = t.pos0 + kk;
