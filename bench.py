@@ -42,8 +42,8 @@ UNIT = "TFLOP/s"
 # while the sources it is compiled from are unchanged (checked by hash;
 # otherwise reported as null)
 TRAFFIC = {"kernel_sources": ['block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu', 'block_diffusion_lm_bdlm_gb300/csrc/common.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/tc_ptx.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/kernels.h'],
-           "sha1": "5dd4721874e775c73ea176173abeb6ff4f326854",
-           "bytes_per_launch": 801709125888 + 406183671296,
+           "sha1": "735c28561a04d12af4283aca6bea2c24d081ed05",
+           "bytes_per_launch": 393825051904 + 205056529408,
            "note": "bwd_tc_kernel on this workload, ncu dram__bytes_read.sum + dram__bytes_write.sum"}
 
 

@@ -9,6 +9,15 @@ The C functions are declared in include/bdlm.h; the Python names are the same:
   bdlm_attn_fwd(q, k, v, block, ...) -> (o, lse)
   bdlm_attn_bwd(q, k, v, o, lse, dO, block, ...) -> (dq, dk, dv)
   bdlm_lse_merge(partials, lses) -> (o, lse)
+  bdlm_attn_fwd_noalloc(...)        forward without a caller workspace
+  bdlm_selftest_timeout(workspace)  device wait-timeout self-test
+Restrictions of a call (see Partial):
+  Partial.window(lo, hi)                     keys at positions [lo, hi) (a clean shard)
+  Partial.window(lo, hi, accumulate=True)    merge into a running (out, lse)
+  Partial.window(lo, hi, q_lo=a, q_hi=b)     only the query rows [a, b)
+  Partial.group(blocks)                      the corrupted rows of a block list
+Packed documents: cu_seqlens (device int32 offsets); ragged last blocks are
+allowed wherever the block size does not divide a half's length.
 """
 from __future__ import annotations
 
