@@ -148,7 +148,8 @@ int main(int argc, char** argv) {
     const int trials = argc > 1 ? std::atoi(argv[1]) : 400;
     int checked = 0;
     for (int it = 0; it < trials; ++it) {
-        const int B = rnd(0, 3) == 0 ? rnd(1, 4) : rnd(1, 96);
+        const int pick = rnd(0, 5);
+        const int B = pick == 0 ? rnd(1, 4) : (pick == 1 ? rnd(129, 300) : rnd(1, 96));  // blocks longer than a tile too
         const int n = rnd(0, 4) == 0 ? B * rnd(1, 6) : rnd(1, 260);
         const int tile_rows = rnd(0, 1) ? 128 : 64;
         // full attention, one sequence

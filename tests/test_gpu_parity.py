@@ -349,6 +349,7 @@ RAGGED = [
     (37, 64, 2, 2, 128),    # B > n: one short block per half
     (129, 128, 2, 1, 128),  # one whole block and one row
     (300, 64, 4, 1, 128),   # several 128-row tiles, short last block
+    (300, 200, 2, 1, 128),  # blocks longer than a 128-row tile, short last block
 ]
 
 
