@@ -59,11 +59,16 @@ def valid_pairs(n, block):
 
 
 def step_flops(w):
-    P = valid_pairs(w.n, w.block)
+    if w.docs:  # packed documents: each document is [clean n_d | corrupted n_d]
+        P = sum(valid_pairs(ln // 2, w.block) for ln in synth.doc_lengths(w))
+    else:
+        P = valid_pairs(w.n, w.block)
     return 4 * w.head_dim * w.heads * P, 10 * w.head_dim * w.heads * P
 
 
 def merge_bytes(w, n_parts):
+    if n_parts == 0:
+        return 0
     rows, per = 2 * w.n, w.heads
     unit = 2 * w.head_dim + 4  # bf16 row of o + fp32 lse
     return rows * per * unit * (n_parts + 1)
@@ -225,11 +230,23 @@ def run_reference(args, rank, world):
 # the CUDA arm
 # ----------------------------------------------------------------------------
 class Step:
+    """One pass of the hot path over one batch: for one sequence, the partial
+    forwards against the clean shards and the local corrupted keys, their
+    merge and the backward; for packed documents (no shards), the forward and
+    backward over cu_seqlens."""
+
     def __init__(self, bd, w, x, dev):
         self.bd, self.w, self.x = bd, w, x
-        n, H, d = w.n, w.heads, w.head_dim
-        L = 2 * n
-        self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+        H, d = w.heads, w.head_dim
+        self.cu = None
+        if w.docs:
+            self.cu = torch.tensor(x.cu_seqlens, dtype=torch.int32, device=dev)
+            L, n_docs = x.cu_seqlens[-1], w.docs
+            self.windows = []
+        else:
+            n = w.n
+            L, n_docs = 2 * n, 1
+            self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
         self.parts = [torch.empty_like(x.q) for _ in self.windows]
         self.plse = [torch.empty((H, L), dtype=torch.float32, device=dev) for _ in self.windows]
         self.o = torch.empty_like(x.q)
@@ -237,8 +254,8 @@ class Step:
         self.dq = torch.empty_like(x.q)
         self.dk = torch.empty_like(x.k)
         self.dv = torch.empty_like(x.v)
-        self.ws_f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d, 1), dtype=torch.uint8, device=dev)
-        self.ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d, 1), dtype=torch.uint8, device=dev)
+        self.ws_f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d, n_docs), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs), dtype=torch.uint8, device=dev)
         self.launches = 0
 
     def run(self, ev=None):
@@ -250,14 +267,18 @@ class Step:
             bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], w.block, part=bd.Partial.window(lo, hi), out=po, lse=pl,
                              workspace=self.ws_f)
             launches += bd.bdlm_last_launch_count()
+        if self.cu is not None:
+            bd.bdlm_attn_fwd(x.q, x.k, x.v, w.block, cu_seqlens=self.cu, out=self.o, lse=self.lse, workspace=self.ws_f)
+            launches += bd.bdlm_last_launch_count()
         if ev:
             ev[1].record()
-        bd.bdlm_lse_merge(self.parts, self.plse, out=self.o, lse=self.lse)
-        launches += bd.bdlm_last_launch_count()
+        if self.windows:
+            bd.bdlm_lse_merge(self.parts, self.plse, out=self.o, lse=self.lse)
+            launches += bd.bdlm_last_launch_count()
         if ev:
             ev[2].record()
-        bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, dq=self.dq, dk=self.dk, dv=self.dv,
-                         workspace=self.ws_b)
+        bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, cu_seqlens=self.cu, dq=self.dq, dk=self.dk,
+                         dv=self.dv, workspace=self.ws_b)
         launches += bd.bdlm_last_launch_count()
         if ev:
             ev[3].record()
@@ -266,8 +287,11 @@ class Step:
     def time_running_merge(self, reps=2):
         """The same windows merged by the forward's epilogue into a running
         fp32 (o, lse) instead of kept as partials and merged (not part of the
-        timed step). Returns the median ms of `reps` runs after one warm-up."""
+        timed step). Returns the median ms of `reps` runs after one warm-up
+        (None for packed documents, which have no windows)."""
         bd, w, x = self.bd, self.w, self.x
+        if not self.windows:
+            return None
         ro = torch.empty(x.q.shape, dtype=torch.float32, device=x.q.device)
         rl = torch.empty_like(self.lse)
 
@@ -332,7 +356,7 @@ def run_cuda(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.BY_NAME[args.workload]
-    if not w.shards:
+    if not w.shards and not w.docs:
         w = synth.Workload(**{**w.__dict__, "shards": 8})
     log(f"[rank {rank}] generating inputs for {w.name}")
     x = synth.make_inputs(w, device="cuda")
@@ -393,7 +417,7 @@ def end_to_end(step, x, flops, args, world, dev):
     for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
         h.copy_(t)
     x_b = synth.Inputs(q=torch.empty_like(x.q), k=torch.empty_like(x.k), v=torch.empty_like(x.v),
-                       do=torch.empty_like(x.do))
+                       do=torch.empty_like(x.do), cu_seqlens=x.cu_seqlens)
     steps = [step, Step(step.bd, step.w, x_b, dev)]
     ins = lambda st: (st.x.q, st.x.k, st.x.v, st.x.do)
     outs = lambda st: (st.o, st.lse, st.dq, st.dk, st.dv)
@@ -473,7 +497,8 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "n_clean": w.n, "n_corrupted": w.n, "block": w.block, "heads": w.heads,
+        "config": {"workload": w.name, "n_clean": w.n, "n_corrupted": w.n, "docs": w.docs or 1,
+                   "rows": x.q.shape[0], "block": w.block, "heads": w.heads,
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "clean_shards": w.shards,
                    "l2": l2_note(x), "parallelism": f"replicas{world}"},
         "roofline": {"kernel": "bdlm_attn_bwd (key-major main kernel + preprocess + dq convert)",
@@ -482,19 +507,21 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
                      "peak_source": f"{peak_kind} bf16_tflops_sustained"},
         "components": {
             "fwd_partials_ms": fwd_ms, "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
-            "merge_ms": mrg_ms, "merge_gbs": mbytes / (mrg_ms / 1e3) / 1e9,
-            "merge_frac_hbm": mbytes / (mrg_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+            "merge_ms": mrg_ms if mbytes else None,
+            "merge_gbs": mbytes / (mrg_ms / 1e3) / 1e9 if mbytes else None,
+            "merge_frac_hbm": mbytes / (mrg_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]) if mbytes else None,
             "bwd_ms": bwd_ms, "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,
             "fwd_frac_bf16": f_fwd / (fwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
             "bwd_frac_bf16": f_bwd / (bwd_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
             "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
-            "fwd_running_merge_ms": run_ms, "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12,
+            "fwd_running_merge_ms": run_ms,
+            "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12 if run_ms else None,
         },
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not w.docs:
         xh = host_group0(x, w)
         rate, pr, dt, nblk = oracle_sample(xh, w, budget_s=args.cpu_budget)
         out["cpu_baseline"] = {
