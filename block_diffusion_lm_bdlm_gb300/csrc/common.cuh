@@ -30,8 +30,7 @@ struct WsHeader {
     int info;      // detail of the first error (e.g. offending document)
     int n_tiles;   // tiles enumerated by the prologue
     int counter;   // dynamic work counter of the main kernel
-    int counter2;  // second counter (second kernel of a call)
-    int pad[59];
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -86,7 +86,6 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         hdr->info = 0;
         hdr->n_tiles = 0;
         hdr->counter = 0;
-        hdr->counter2 = 0;
         s_carry = 0;
     }
     for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
