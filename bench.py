@@ -42,8 +42,8 @@ UNIT = "TFLOP/s"
 # while the sources it is compiled from are unchanged (checked by hash;
 # otherwise reported as null)
 TRAFFIC = {"kernel_sources": ['block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu', 'block_diffusion_lm_bdlm_gb300/csrc/common.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/tc_ptx.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/kernels.h'],
-           "sha1": "735c28561a04d12af4283aca6bea2c24d081ed05",
-           "bytes_per_launch": 393825051904 + 205056529408,
+           "sha1": "e1352b8ba7ec9e14bea9c857e8a767840a958389",
+           "bytes_per_launch": 399730392320 + 211021425664,
            "note": "bwd_tc_kernel on this workload, ncu dram__bytes_read.sum + dram__bytes_write.sum"}
 
 
@@ -72,6 +72,15 @@ def merge_bytes(w, n_parts):
     rows, per = 2 * w.n, w.heads
     unit = 2 * w.head_dim + 4  # bf16 row of o + fp32 lse
     return rows * per * unit * (n_parts + 1)
+
+
+def mufu_exp_peak(clocks):
+    """Exponentials per second the special-function units can issue: 16 ex2
+    per clock per SM (4 per SM sub-partition), times the SM count, at the
+    median SM clock sampled under load (the maximum clock when no sample)."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070
+    return 16.0 * sms * float(mhz) * 1e6
 
 
 def load_peaks():
@@ -389,6 +398,7 @@ def run_cuda(args, rank, world, local):
     mrg_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     bwd_ms = statistics.median(e[2].elapsed_time(e[3]) for e in evs)
     bwd_mean_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / len(evs)
+    step_ms = sorted(e[0].elapsed_time(e[3]) for e in evs)
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     value = flops * world * args.steps / (total_ms / 1e3) / 1e12
@@ -401,7 +411,7 @@ def run_cuda(args, rank, world, local):
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms)
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -488,7 +498,7 @@ def l2_note(x):
 
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms):
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -516,6 +526,10 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
             "fwd_running_merge_ms": run_ms,
             "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12 if run_ms else None,
+            "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
+            # the forward's secondary bound: one exponential per valid (row, key) pair and head
+            "fwd_exp_per_s": f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3),
+            "fwd_exp_frac_mufu": (f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3)) / mufu_exp_peak(clocks),
         },
         "e2e": e2e,
         "gpu_launches": launches,
