@@ -16,5 +16,6 @@ from .bdlm_oracle import (  # noqa: F401
     lse_merge,
     mask_rows,
     partial_attention,
+    task_attention,
     valid_pairs,
 )

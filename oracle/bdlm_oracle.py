@@ -290,6 +290,43 @@ def group_attention(q_g, k_g, v_g, n, block, blocks, scale, do=None):
     return out
 
 
+# ----------------------------------------------------------------------------
+# Token-level task lists ("Efficient Long-context Language Model Training by
+# Core Attention Disaggregation", abstract: core attention is stateless and
+# composes over fused batches of token-level shards of arbitrary lengths).
+# A task is one query row range of one sequence against one key window of the
+# same sequence, under that sequence's BDLM mask; its result is a partial (o,
+# lse) for those rows, which a log-sum-exp merge combines with the partials of
+# the same rows against other keys.
+# ----------------------------------------------------------------------------
+def task_attention(q, k, v, block, scale, tasks, n_slots, o=None, lse=None):
+    """Run a list of tasks over packed sequences.
+
+    q [L, H, d], k/v [L, Hk, d] hold every row. A task is a dict with
+    seq_start, n (its sequence is rows [seq_start, seq_start + 2n), clean then
+    corrupted), q_lo, q_hi, key_lo, key_hi (positions within the sequence) and
+    slot. Task t writes the partial of its rows against its keys into
+    o[slot, seq_start + q_lo : seq_start + q_hi] and the matching lse columns;
+    rows no task of a slot covers keep their value in the given o / lse
+    (default: NaN). Returns o [S, L, H, d], lse [S, H, L].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    L, H, d = q.shape
+    o = np.full((n_slots, L, H, d), np.nan) if o is None else np.array(o, dtype=np.float64)
+    lse = np.full((n_slots, H, L), np.nan) if lse is None else np.array(lse, dtype=np.float64)
+    for t in tasks:
+        s0, n = t["seq_start"], t["n"]
+        qa, qb = s0 + t["q_lo"], s0 + t["q_hi"]
+        ka, kb = s0 + t["key_lo"], s0 + t["key_hi"]
+        r = partial_attention(q[qa:qb], k[ka:kb], v[ka:kb], n, block, t["key_lo"], t["key_hi"], scale,
+                              q_lo=t["q_lo"], q_hi=t["q_hi"])
+        o[t["slot"], qa:qb] = r["o"]
+        lse[t["slot"], :, qa:qb] = r["lse"]
+    return o, lse
+
+
 def valid_pairs(n, block):
     """Closed form of the mask's population per head for one sequence.
     With n = nb B + r: the clean rows of a full block b see (b+1)B keys, the

@@ -291,6 +291,44 @@ def test_row_range_by_key_window_grid(n, block):
     np.testing.assert_allclose(dv, full["dv"], atol=1e-12)
 
 
+def test_task_list_over_packed_sequences():
+    # Token-level tasks over two packed sequences of different (ragged) lengths:
+    # each sequence's rows cut into row ranges and its keys into windows, task
+    # (range, window w) writing slot w; per sequence, merging the slots gives
+    # that sequence's attention alone, and the row ranges no task of a slot
+    # covers keep their sentinel.
+    H, Hk, d, block = 4, 2, 8, 4
+    scale = 0.4
+    ns = [13, 22]
+    rows = 2 * sum(ns)
+    rng = np.random.default_rng(81)
+    q = rng.standard_normal((rows, H, d))
+    k = rng.standard_normal((rows, Hk, d))
+    v = rng.standard_normal((rows, Hk, d))
+    starts = [0, 2 * ns[0]]
+    tasks, n_slots = [], 3
+    for s0, n in zip(starts, ns):
+        row_cuts = [0, 5, n + 2, 2 * n]
+        key_cuts = [0, n - 3, n + 1, 2 * n]
+        for qa, qb in zip(row_cuts[:-1], row_cuts[1:]):
+            for w, (ka, kb) in enumerate(zip(key_cuts[:-1], key_cuts[1:])):
+                tasks.append(dict(seq_start=s0, n=n, q_lo=qa, q_hi=qb, key_lo=ka, key_hi=kb, slot=w))
+    o, lse = oracle.task_attention(q, k, v, block, scale, tasks, n_slots)
+    assert not np.isnan(o).any() and not np.isnan(lse).any()
+    om, lm = oracle.lse_merge(o, lse)
+    for s0, n in zip(starts, ns):
+        alone = oracle.dense_bdlm_attention(q[s0:s0 + 2 * n], k[s0:s0 + 2 * n], v[s0:s0 + 2 * n], n, block, scale)
+        np.testing.assert_allclose(om[s0:s0 + 2 * n], alone["o"], atol=1e-12)
+        np.testing.assert_allclose(lm[:, s0:s0 + 2 * n], alone["lse"], atol=1e-12)
+    # the clean rows of a sequence see no corrupted key: o = 0, lse = -inf there
+    n = ns[1]
+    s0 = starts[1]
+    t = [dict(seq_start=s0, n=n, q_lo=0, q_hi=n, key_lo=n, key_hi=2 * n, slot=1)]
+    o2, l2 = oracle.task_attention(q, k, v, block, scale, t, 2)
+    assert np.all(o2[1, s0:s0 + n] == 0.0) and np.all(l2[1, :, s0:s0 + n] == -np.inf)
+    assert np.isnan(o2[0]).all() and np.isnan(o2[1, :s0]).all() and np.isnan(o2[1, s0 + n:]).all()
+
+
 def test_merge_special_cases():
     rng = np.random.default_rng(70)
     R, H, d = 5, 2, 3
