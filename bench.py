@@ -256,8 +256,16 @@ class Step:
             n = w.n
             L, n_docs = 2 * n, 1
             self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
-        self.parts = [torch.empty_like(x.q) for _ in self.windows]
-        self.plse = [torch.empty((H, L), dtype=torch.float32, device=dev) for _ in self.windows]
+        # the partials as one [P, L, H, d] buffer (and [P, H, L] lse): the
+        # window calls write its slices, a task list writes its slots
+        P = len(self.windows)
+        self.parts_all = torch.empty((P,) + tuple(x.q.shape), dtype=x.q.dtype, device=dev) if P else None
+        self.plse_all = torch.empty((P, H, L), dtype=torch.float32, device=dev) if P else None
+        self.parts = [self.parts_all[i] for i in range(P)]
+        self.plse = [self.plse_all[i] for i in range(P)]
+        self.tasks = [bd.Task(0, w.n, 0, 2 * w.n, lo, hi, i) for i, (lo, hi) in enumerate(self.windows)]
+        self.ws_t = torch.empty(max(bd.bdlm_attn_fwd_tasks_workspace_bytes(self.tasks), 256), dtype=torch.uint8,
+                                device=dev) if P else None
         self.o = torch.empty_like(x.q)
         self.lse = torch.empty((H, L), dtype=torch.float32, device=dev)
         self.dq = torch.empty_like(x.q)
@@ -292,6 +300,30 @@ class Step:
         if ev:
             ev[3].record()
         self.launches += launches
+
+    def time_task_list(self, reps=3):
+        """The same partial forwards as one task list (one attention launch
+        over all windows, into the same partial buffers; not part of the timed
+        step). Returns the median ms of `reps` runs after one warm-up (None
+        for packed documents)."""
+        bd, w, x = self.bd, self.w, self.x
+        if not self.windows:
+            return None
+
+        def run():
+            bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, w.block, self.tasks, len(self.tasks), out=self.parts_all,
+                                   lse=self.plse_all, workspace=self.ws_t)
+
+        run()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
 
     def time_running_merge(self, reps=2):
         """The same windows merged by the forward's epilogue into a running
@@ -407,11 +439,12 @@ def run_cuda(args, rank, world, local):
     achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     run_ms = step.time_running_merge()
+    task_ms = step.time_task_list()
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms)
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -498,7 +531,7 @@ def l2_note(x):
 
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms):
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -526,6 +559,8 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "flops_fwd": f_fwd, "flops_bwd": f_bwd, "merge_bytes": mbytes,
             "fwd_running_merge_ms": run_ms,
             "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12 if run_ms else None,
+            "fwd_task_list_ms": task_ms,
+            "fwd_task_list_tflops": f_fwd / (task_ms / 1e3) / 1e12 if task_ms else None,
             "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
             # the forward's secondary bound: one exponential per valid (row, key) pair and head
             "fwd_exp_per_s": f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3),

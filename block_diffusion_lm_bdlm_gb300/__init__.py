@@ -9,6 +9,8 @@ The C functions are declared in include/bdlm.h; the Python names are the same:
   bdlm_attn_fwd(q, k, v, block, ...) -> (o, lse)
   bdlm_attn_bwd(q, k, v, o, lse, dO, block, ...) -> (dq, dk, dv)
   bdlm_lse_merge(partials, lses) -> (o, lse)
+  bdlm_attn_fwd_tasks(q, k, v, block, tasks, n_slots) -> (o [S,L,H,d], lse [S,H,L])
+                                    a token-level task list in one launch
   bdlm_attn_fwd_noalloc(...)        forward without a caller workspace
   bdlm_selftest_timeout(workspace)  device wait-timeout self-test
 Restrictions of a call (see Partial):
@@ -31,7 +33,7 @@ import torch
 from .build import LIB
 
 __all__ = [
-    "BDLMError", "Partial", "bdlm_attn_fwd", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
+    "BDLMError", "Partial", "Task", "bdlm_attn_fwd", "bdlm_attn_fwd_tasks", "bdlm_attn_fwd_tasks_workspace_bytes", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_last_launch_count",
     "bdlm_selftest_timeout", "load_library", "EXPORTED_SYMBOLS",
 ]
@@ -45,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_attn_fwd", "bdlm_attn_bwd",
     "bdlm_lse_merge", "bdlm_read_error", "bdlm_status_string", "bdlm_last_launch_count",
     "bdlm_attn_fwd_noalloc",
+    "bdlm_attn_fwd_tasks_workspace_bytes", "bdlm_attn_fwd_tasks",
     "bdlm_selftest_timeout",
 )
 
@@ -106,6 +109,33 @@ class Partial:
         return _CPartial(self.kind, nb, self.key_lo, self.key_hi, ptr, flags, o_dtype, self.q_lo, self.q_hi)
 
 
+class _CTask(ctypes.Structure):
+    _fields_ = [("seq_start", ctypes.c_int64), ("n", ctypes.c_int64), ("q_lo", ctypes.c_int64),
+                ("q_hi", ctypes.c_int64), ("key_lo", ctypes.c_int64), ("key_hi", ctypes.c_int64),
+                ("slot", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class Task:
+    """One token-level task: the query positions [q_lo, q_hi) of the sequence
+    at rows [seq_start, seq_start + 2n) against its key positions
+    [key_lo, key_hi), written to output slot `slot`."""
+    seq_start: int
+    n: int
+    q_lo: int
+    q_hi: int
+    key_lo: int
+    key_hi: int
+    slot: int = 0
+
+
+def _task_array(tasks: Sequence[Task]):
+    arr = (_CTask * len(tasks))()
+    for i, t in enumerate(tasks):
+        arr[i] = _CTask(t.seq_start, t.n, t.q_lo, t.q_hi, t.key_lo, t.key_hi, t.slot, 0)
+    return arr
+
+
 _lib = None
 
 
@@ -139,6 +169,11 @@ def load_library() -> ctypes.CDLL:
     lib.bdlm_status_string.restype = ctypes.c_char_p
     lib.bdlm_last_launch_count.argtypes = []
     lib.bdlm_last_launch_count.restype = ctypes.c_int
+    lib.bdlm_attn_fwd_tasks_workspace_bytes.argtypes = [ctypes.POINTER(_CTask), i32]
+    lib.bdlm_attn_fwd_tasks_workspace_bytes.restype = sz
+    lib.bdlm_attn_fwd_tasks.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
+                                        ctypes.POINTER(_CTask), i32, i32, i32, vp, sz, vp]
+    lib.bdlm_attn_fwd_tasks.restype = ctypes.c_int
     lib.bdlm_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
     lib.bdlm_selftest_timeout.restype = ctypes.c_int
     _lib = lib
@@ -236,6 +271,45 @@ def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=No
                            Hk, d, cu_ptr, n_docs, softmax_scale, cpart, workspace.data_ptr(),
                            workspace.numel(), _stream(stream))
     _check(st, "bdlm_attn_fwd")
+    return out, lse
+
+
+def bdlm_attn_fwd_tasks_workspace_bytes(tasks: Sequence[Task]) -> int:
+    return int(load_library().bdlm_attn_fwd_tasks_workspace_bytes(_task_array(tasks), len(tasks)))
+
+
+def bdlm_attn_fwd_tasks(q, k, v, block: int, tasks: Sequence[Task], n_slots: int, *, softmax_scale: float = 0.0,
+                        out=None, lse=None, workspace=None, stream=None):
+    """Every task's partial forward in one launch. q [L,H,d], k/v [L,Hk,d]
+    hold every row. Returns (o [n_slots,L,H,d], lse [n_slots,H,L]): task t
+    fills slot t.slot at its rows; rows no task of a slot covers keep what
+    `out` / `lse` held (fresh outputs start as o = 0, lse = -inf, so merging
+    the slots with bdlm_lse_merge combines tasks that split a row's keys).
+    `out` may be fp32 to keep the partials unrounded."""
+    lib = load_library()
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(nm, t)
+    L, H, d = q.shape
+    Hk = k.shape[1]
+    if out is None:
+        out = torch.zeros((n_slots, L, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.full((n_slots, H, L), float("-inf"), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (n_slots, L, H, d) \
+            or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 or fp32 CUDA tensor [n_slots, L, H, d]")
+    if tuple(lse.shape) != (n_slots, H, L) or lse.dtype != torch.float32 or not lse.is_cuda \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [n_slots, H, L]")
+    arr = _task_array(tasks)
+    ws_bytes = lib.bdlm_attn_fwd_tasks_workspace_bytes(arr, len(tasks))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    o_dtype = BDLM_F32 if out.dtype == torch.float32 else BDLM_BF16
+    st = lib.bdlm_attn_fwd_tasks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L, block,
+                                 H, Hk, d, softmax_scale, arr, len(tasks), n_slots, o_dtype, workspace.data_ptr(),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "bdlm_attn_fwd_tasks")
     return out, lse
 
 

@@ -19,7 +19,7 @@
 
 namespace bdlm {
 
-enum Mode : int { MODE_FULL = 0, MODE_WINDOW = 1, MODE_GROUP = 2 };
+enum Mode : int { MODE_FULL = 0, MODE_WINDOW = 1, MODE_GROUP = 2, MODE_TASKS = 3 };
 
 // Status codes written to the device error word (same values as bdlm.h).
 enum DevStatus : int { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_CHECK = 6 };
@@ -34,6 +34,18 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// One token-level task of a task-list forward, as the kernels read it: the
+// query positions [q_lo, q_hi) of the sequence at rows [seq_start,
+// seq_start + 2n) of q, k, v against its key positions [kw_lo, kw_hi);
+// results go to output slot `slot`.
+struct TaskRec {
+    int seq_start, n;
+    int kw_lo, kw_hi;
+    int q_lo, q_hi;
+    int slot, pad;
+};
+static_assert(sizeof(TaskRec) == 32, "task record is 32 bytes");
+
 // How the rows of a call map to sequence positions.
 struct Layout {
     int mode;
@@ -46,6 +58,8 @@ struct Layout {
     long long L;       // rows of the full concatenation
     const int* blocks; // MODE_GROUP: device list of corrupted block ids
     int n_blocks;
+    const TaskRec* tasks;  // MODE_TASKS: device task records
+    int n_tasks;
 };
 
 // One tile of consecutive rows that never straddles a document half.
@@ -53,8 +67,9 @@ struct Layout {
 struct Tile {
     int doc_start;  // first row of the document (0 for window / group)
     int n;          // clean length of the document
-    int pos0;       // document position (full/window) or list row (group) of row 0
+    int pos0;       // document position (full/window/tasks) or list row (group) of row 0
     int nrows;      // valid rows (<= tile height)
+    int task;       // MODE_TASKS: index of the tile's task
 };
 
 struct Span {
@@ -99,9 +114,17 @@ __host__ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile&
     }
     const int n = t.n;
     const int pos = t.pos0 + r;
-    const int kw_lo = lay.mode == MODE_WINDOW ? lay.kw_lo : 0;
-    const int kw_hi = lay.mode == MODE_WINDOW ? lay.kw_hi : 2 * n;
-    const int kbase = t.doc_start - kw_lo;
+    // key window and k row of key position 0: a window's k/v hold only its
+    // keys; a task's k/v hold every row, its window bounds the positions
+    int kw_lo = 0, kw_hi = 2 * n, kbase = t.doc_start;
+    if (lay.mode == MODE_WINDOW) {
+        kw_lo = lay.kw_lo;
+        kw_hi = lay.kw_hi;
+        kbase -= kw_lo;
+    } else if (lay.mode == MODE_TASKS) {
+        kw_lo = ld_ro(&lay.tasks[t.task].kw_lo);
+        kw_hi = ld_ro(&lay.tasks[t.task].kw_hi);
+    }
     int pref_hi, dlo = 0, dhi = 0;
     if (pos < n) {
         pref_hi = (pos / B + 1) * B;
@@ -192,8 +215,8 @@ __host__ __device__ __forceinline__ int group_count_le(const Layout& lay, int b)
     return lo;
 }
 
-// q row of row position p of a tile (full: document start + position;
-// window: position - q_lo; group: the list row itself).
+// q row of row position p of a tile (full and tasks: sequence start +
+// position; window: position - q_lo; group: the list row itself).
 __host__ __device__ __forceinline__ int q_row_of(const Layout& lay, const Tile& t, int p) {
     return t.doc_start + p - (lay.mode == MODE_WINDOW ? lay.q_lo : 0);
 }

@@ -178,7 +178,8 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
 // warp-collective, so every branch around them is warp-uniform.
 template <int D>
 __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a, const uint64_t* bar, uint32_t tmem,
-                                             int i, uint32_t tb, volatile int* abort) {
+                                             int i, uint32_t tb, volatile int* abort,
+                                             const int* item_p) {
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16;
     const uint32_t tS = tmem + i * 128 + lane_base;
@@ -274,8 +275,16 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
     }
     const bool have_o = ok && c.nk > 0;  // warp-uniform
     const bool store = row < c.T.nrows;
-    const long long ooff = ((long long)c.q_row0 + row) * ((long long)a.H * D) + (long long)h * D;
-    const long long lidx = (long long)h * a.Lq + c.q_row0 + row;
+    // o [slots, Lq, H, D], lse [slots, H, Lq]; a task list's tile takes the
+    // slot of its task (looked up again from the item number, which stays in
+    // shared memory until every role has finished the item)
+    int slot = 0;
+    if (a.lay.mode == MODE_TASKS) {
+        const int n_pairs = a.Hk * ((a.G + 1) / 2);
+        slot = ld_ro(&a.lay.tasks[ld_ro(&a.table[*item_p / n_pairs].task)].slot);
+    }
+    const long long ooff = ((long long)slot * a.Lq + c.q_row0 + row) * ((long long)a.H * D) + (long long)h * D;
+    const long long lidx = ((long long)slot * a.H + h) * a.Lq + c.q_row0 + row;
     // this call's row: lse in base 2, o = (unnormalised O) * cw
     const float l2w = l > 0.f ? m_use + __log2f(l) : -INFINITY;
     float cw = l > 0.f ? 1.f / l : 0.f, ca = 0.f, l2out = l2w;
@@ -438,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int item = s_item;
             if (item >= n_items) break;
             const ItemCtx c = decode(a, ranges, item, n_pairs, per_kv);
-            if (wg == 0 || c.two) softmax_rows<D>(c, a, bar, tmem, wg, wg == 0 ? t_base : t_base1, abort);
+            if (wg == 0 || c.two) softmax_rows<D>(c, a, bar, tmem, wg, wg == 0 ? t_base : t_base1, abort, &s_item);
             t_base += c.nk;
             if (c.two) t_base1 += c.nk;
         }

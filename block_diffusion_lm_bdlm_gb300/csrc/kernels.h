@@ -13,6 +13,7 @@ struct WsCarve {
     int* cost;      // per-tile cost (prologue scratch)
     TileRange* ranges;   // key ranges of the ordered tiles (forward)
     TileRange* rng_tmp;  // key ranges of the unordered tiles (prologue scratch)
+    TaskRec* tasks;      // task list (task-list forward)
     int max_tiles;
     float* D;       // backward: rowsum(dO * o), [H, L]
     float* dqacc;   // backward: fp32 dq accumulator, [L, H, d]
@@ -72,6 +73,9 @@ constexpr int kBwdKeyTile = 64;     // warp-level backward (head_dim 64)
 constexpr int kBwdTcKeyTile = 128;  // tensor-core backward (head_dim 128)
 constexpr int kBwdQTile = 64;
 
+// Task records per upload launch (kernel parameters stay under 32 KB).
+constexpr int kTaskUploadChunk = 960;
+int launch_task_upload(const TaskRec* host, int n, TaskRec* dst, cudaStream_t st);  // returns launches
 void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, const WsCarve& ws,
                       cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st, int* launches);

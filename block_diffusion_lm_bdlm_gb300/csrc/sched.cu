@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kBuckets = 8192;
+constexpr int kTaskGroups = 64;  // task-order levels among tiles of equal cost
 
 __device__ int block_exclusive_scan(int x, int* total, int* sbuf) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -66,6 +67,9 @@ __device__ int fwd_cost(const TileRange& g, int kn) {
     return (g.r1_hi - g.r1_lo + kn - 1) / kn + (g.r2_hi - g.r2_lo + kn - 1) / kn;
 }
 
+// Tiles of `rows` rows covering positions [lo, hi).
+__device__ __forceinline__ int run_tiles(int lo, int hi, int rows) { return hi > lo ? (hi - lo + rows - 1) / rows : 0; }
+
 // Cost of a backward key tile, in query rows that see it.
 __device__ int bwd_cost(const Layout& lay, const Tile& t) {
     const KeyRows r = key_tile_rows(lay, t);
@@ -75,7 +79,7 @@ __device__ int bwd_cost(const Layout& lay, const Tile& t) {
 __global__ void __launch_bounds__(kThreads, 1)
 enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table, Tile* tmp,
                  int* cost_tmp, TileRange* ranges, TileRange* rng_tmp, WsHeader* hdr, int max_tiles,
-                 int cost_shift) {
+                 int cost_shift, int task_groups) {
     __shared__ int hist[kBuckets];
     __shared__ int sbuf[96];
     __shared__ int s_carry;
@@ -145,6 +149,43 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         }
         if (tid == 0) s_carry = nc + nx;
         __syncthreads();
+    } else if (lay.mode == MODE_TASKS) {
+        // tasks in chunks of kThreads: scan the per-task tile counts (each
+        // task's query positions in two runs split at its clean/corrupted
+        // boundary), then let every thread fill tiles, finding its task by
+        // binary search over the chunk's tile offsets
+        for (int base = 0; base < lay.n_tasks; base += kThreads) {
+            const int ti = base + tid;
+            const int nt = imin(kThreads, lay.n_tasks - base);
+            int cnt = 0;
+            if (ti < lay.n_tasks) {
+                const TaskRec r = lay.tasks[ti];
+                cnt = run_tiles(r.q_lo, imin(r.q_hi, r.n), tile_rows) + run_tiles(imax(r.q_lo, r.n), r.q_hi, tile_rows);
+            }
+            int total;
+            const int off = block_exclusive_scan(cnt, &total, sbuf);
+            s_off[tid] = off;
+            __syncthreads();
+            const int carry = s_carry;
+            for (int i = tid; i < total; i += kThreads) {
+                int lo = 0, hi = nt - 1;  // last task whose offset <= i
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+                }
+                const TaskRec r = lay.tasks[base + lo];
+                const int li = i - s_off[lo];
+                const int c_hi = imin(r.q_hi, r.n);
+                const int nc = run_tiles(r.q_lo, c_hi, tile_rows);
+                const int p0 = li < nc ? r.q_lo + li * tile_rows : imax(r.q_lo, r.n) + (li - nc) * tile_rows;
+                const int end = li < nc ? c_hi : r.q_hi;
+                const int idx = carry + i;
+                if (idx < max_tiles) tmp[idx] = Tile{r.seq_start, r.n, p0, imin(tile_rows, end - p0), base + lo};
+            }
+            __syncthreads();
+            if (tid == 0) s_carry = carry + total;
+            __syncthreads();
+        }
     } else if (lay.mode == MODE_GROUP) {
         const int rows = lay.n_blocks * lay.B;
         const int nt = (rows + tile_rows - 1) / tile_rows;
@@ -207,7 +248,11 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         } else {
             c = bwd_cost(lay, t);
         }
-        c = imin(c >> cost_shift, kBuckets - 1);
+        c = c >> cost_shift;
+        // task lists: among tiles of equal cost, earlier tasks first, so
+        // that the CTAs running side by side mostly share one task's keys
+        if (task_groups > 1) c = c * task_groups + (task_groups - 1 - (int)((long long)t.task * task_groups / lay.n_tasks));
+        c = imin(c, kBuckets - 1);
         cost_tmp[i] = c;
         atomicAdd(&hist[c], 1);
     }
@@ -239,17 +284,44 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
     if (tid == 0) hdr->n_tiles = n_tiles;
 }
 
+// Task records reach the device as kernel parameters (no host-to-device
+// copy, and a captured launch keeps them by value).
+struct TaskChunk {
+    int count;
+    int pad[7];
+    TaskRec rec[kTaskUploadChunk];
+};
+
+__global__ void task_upload_kernel(const __grid_constant__ TaskChunk c, TaskRec* dst) {
+    for (int i = threadIdx.x; i < c.count; i += blockDim.x) dst[i] = c.rec[i];
+}
+
 }  // namespace
+
+int launch_task_upload(const TaskRec* host, int n, TaskRec* dst, cudaStream_t st) {
+    int launches = 0;
+    for (int base = 0; base < n; base += kTaskUploadChunk) {
+        TaskChunk c;
+        c.count = imin(kTaskUploadChunk, n - base);
+        for (int i = 0; i < 7; ++i) c.pad[i] = 0;
+        for (int i = 0; i < c.count; ++i) c.rec[i] = host[base + i];
+        task_upload_kernel<<<1, 256, 0, st>>>(c, dst + base);
+        ++launches;
+    }
+    return launches;
+}
 
 void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, const WsCarve& ws,
                       cudaStream_t st) {
-    // keep the costs inside the histogram for very long sequences
+    // keep the costs inside the histogram for very long sequences (a task
+    // list's lay.n is its longest sequence), with room for the task order
+    const int groups = lay.mode == MODE_TASKS ? imin(lay.n_tasks, kTaskGroups) : 1;
     int shift = 0;
     long long max_cost = kind == 0 ? (2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n)) / key_tile + 4
                                    : 2 * (long long)(lay.mode == MODE_FULL && lay.cu ? lay.L : lay.n);
-    while ((max_cost >> shift) >= kBuckets) ++shift;
+    while (((max_cost >> shift) + 1) * groups > kBuckets) ++shift;
     enumerate_kernel<<<1, kThreads, 0, st>>>(lay, tile_rows, key_tile, kind, ws.table, ws.tmp, ws.cost,
-                                             ws.ranges, ws.rng_tmp, ws.hdr, ws.max_tiles, shift);
+                                             ws.ranges, ws.rng_tmp, ws.hdr, ws.max_tiles, shift, groups);
 }
 
 }  // namespace bdlm

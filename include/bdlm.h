@@ -178,6 +178,63 @@ BDLM_API int bdlm_attn_fwd_noalloc(const void* q, const void* k, const void* v, 
                   const bdlm_partial* part, bdlm_stream_t stream);
 
 /*
+ * Token-level task lists ("Efficient Long-context Language Model Training by
+ * Core Attention Disaggregation", abstract: core attention is stateless and
+ * composes over fused batches of token-level shards of arbitrary lengths).
+ *
+ * A task is the query rows at positions [q_lo, q_hi) of one sequence against
+ * that sequence's keys at positions [key_lo, key_hi), under the sequence's
+ * BDLM mask. The sequence is [clean n | corrupted n] at rows [seq_start,
+ * seq_start + 2n) of q, k and v, which hold all L rows. The tasks of one list
+ * may come from different sequences of different lengths (B need not divide
+ * n) and may cut one sequence's rows and keys in any way.
+ */
+typedef struct {
+    int64_t seq_start;       /* first row of the task's sequence in q, k, v       */
+    int64_t n;               /* its clean length: rows [seq_start, seq_start + 2n) */
+    int64_t q_lo, q_hi;      /* query positions, 0 <= q_lo < q_hi <= 2n            */
+    int64_t key_lo, key_hi;  /* key positions, 0 <= key_lo < key_hi <= 2n          */
+    int32_t slot;            /* output slot, 0 <= slot < n_slots                   */
+    int32_t reserved;        /* must be 0                                          */
+} bdlm_task;
+
+/* Workspace (bytes, 256-byte aligned) of a task-list forward over this HOST
+ * task array; 0 if n_tasks is outside [1, 65536] or a task has an empty or
+ * negative query range or a non-positive n. */
+BDLM_API size_t bdlm_attn_fwd_tasks_workspace_bytes(const bdlm_task* tasks, int32_t n_tasks);
+
+/*
+ * bdlm_attn_fwd_tasks - the partial forward of every task of a list, in one
+ * attention launch (after a prologue that takes the tasks to the device as
+ * kernel parameters and orders their tiles: heaviest first, and among tiles
+ * of equal cost earlier tasks first).
+ *
+ *   q, k, v    bf16 [L, H, d], [L, Hk, d]: every row.
+ *   o          n_slots consecutive [L, H, d] arrays of o_dtype (BDLM_BF16 or
+ *              BDLM_F32).
+ *   lse        n_slots consecutive fp32 [H, L] arrays.
+ *   tasks      HOST array of n_tasks tasks (1 .. 65536), read during the call;
+ *              it may be reused or freed when the call returns.
+ *   n_slots    1 .. 1024.
+ *   workspace  >= bdlm_attn_fwd_tasks_workspace_bytes(tasks, n_tasks).
+ *
+ * Task t writes o[slot_t] and lse[slot_t] at rows seq_start + [q_lo, q_hi):
+ * the partial result of those rows against the task's keys (o = 0 and
+ * lse = -inf for rows that see none of them). Rows that no task of a slot
+ * covers are left as they were. Tasks that split one row's keys go to
+ * different slots, and bdlm_lse_merge over the slots (with lse = -inf set
+ * beforehand where a slot has no task) combines them. Tasks of one slot must
+ * not share query rows, since they would write the same outputs: such a list
+ * returns BDLM_ERR_INVALID_ARG, as does a task whose sequence does not lie in
+ * [0, L), whose ranges break the bounds above, or whose reserved field is not
+ * 0.
+ */
+BDLM_API int bdlm_attn_fwd_tasks(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                  float softmax_scale, const bdlm_task* tasks, int32_t n_tasks, int32_t n_slots,
+                  int32_t o_dtype, void* workspace, size_t workspace_bytes, bdlm_stream_t stream);
+
+/*
  * Backward: given q, k, v, the forward's o and lse, and the upstream gradient
  * dO, writes dq [Lq, H, d], dk [Lk, Hk, d], dv [Lk, Hk, d] (bf16), the
  * gradients of softmax(QK^T)V under the BDLM mask ("Efficient Long-context

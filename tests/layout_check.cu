@@ -1,8 +1,8 @@
 // layout_check.cu - host-side check of the kernels' layout index math
 // (block_diffusion_lm_bdlm_gb300/csrc/common.cuh) against a pairwise restatement of
 // the BDLM mask, over many random sequence lengths, block sizes, key windows,
-// query row ranges and block groups. Built and run by tests/test_layout_math.py;
-// no GPU is used.
+// query row ranges, block groups and task lists. Built and run by
+// tests/test_layout_math.py; no GPU is used.
 //
 // The mask (Block Parallelism abstract; rit.work CSBP post, first section), per
 // (query position p, key position j) of one [clean n | corrupted n] sequence,
@@ -142,6 +142,82 @@ void check_backward(const Call& c, int key_rows_per_tile) {
     }
 }
 
+// Task lists: tasks over packed sequences, each a query position range of one
+// sequence against a key window of it; k rows are the packed rows. Every tile
+// of every task must see exactly the keys of its own sequence that lie in the
+// task's window and that the mask shows the row, each once.
+void check_tasks(int tile_rows) {
+    const int n_seq = rnd(1, 4);
+    std::vector<int> seq_start, seq_n;
+    int L = 0;
+    const int B = rnd(0, 3) == 0 ? rnd(129, 200) : rnd(1, 40);
+    for (int i = 0; i < n_seq; ++i) {
+        seq_start.push_back(L);
+        seq_n.push_back(rnd(1, 220));
+        L += 2 * seq_n.back();
+    }
+    std::vector<TaskRec> tasks;
+    const int nt = rnd(1, 8);
+    for (int i = 0; i < nt; ++i) {
+        const int sq = rnd(0, n_seq - 1), n = seq_n[sq];
+        TaskRec r{};
+        r.seq_start = seq_start[sq];
+        r.n = n;
+        r.q_lo = rnd(0, 2 * n - 1);
+        r.q_hi = rnd(r.q_lo + 1, 2 * n);
+        r.kw_lo = rnd(0, 2 * n - 1);
+        r.kw_hi = rnd(r.kw_lo + 1, 2 * n);
+        r.slot = i;
+        tasks.push_back(r);
+    }
+    Layout lay;
+    std::memset(&lay, 0, sizeof(lay));
+    lay.mode = MODE_TASKS;
+    lay.B = B;
+    lay.L = L;
+    lay.n_docs = 1;
+    lay.tasks = tasks.data();
+    lay.n_tasks = nt;
+    const int BN = 128;
+    for (int ti = 0; ti < nt; ++ti) {
+        const TaskRec& r = tasks[ti];
+        for (const Tile& t0 : tiles(r.q_lo, r.q_hi, r.n, tile_rows, r.n)) {
+            Tile t = t0;
+            t.doc_start = r.seq_start;
+            t.task = ti;
+            const TileRange g = tile_range(lay, t);
+            const int n1 = (g.r1_hi - g.r1_lo + BN - 1) / BN, n2 = (g.r2_hi - g.r2_lo + BN - 1) / BN;
+            for (int row = 0; row < t.nrows; ++row) {
+                const int p = t.pos0 + row;
+                if (q_row_of(lay, t, p) != r.seq_start + p) fail("task q row", r.n, B, p, ti, 0);
+                const Span s = row_span(lay, t, row);
+                std::vector<int> counted(L, 0);
+                for (int j = 0; j < n1 + n2; ++j) {
+                    const bool pre = j < n1;
+                    const int k0 = pre ? g.r1_lo + j * BN : g.r2_lo + (j - n1) * BN;
+                    const bool full = pre && k0 >= g.full_lo && k0 + BN <= g.full_hi;
+                    const RelInterval ri = range_interval(s, pre, k0);
+                    for (int e = 0; e < BN; ++e) {
+                        const int kr = k0 + e;
+                        const bool sees = full || rel_sees(ri, e);
+                        if (kr < 0 || kr >= L) {
+                            if (sees && !full) fail("task mask outside k", r.n, B, p, kr, j);
+                            continue;
+                        }
+                        if (sees) ++counted[kr];
+                    }
+                }
+                for (int kr = 0; kr < L; ++kr) {
+                    const int j = kr - r.seq_start;
+                    const bool want = j >= r.kw_lo && j < r.kw_hi && visible(p, j, r.n, B);
+                    if (counted[kr] != (want ? 1 : 0)) fail("task pair count", r.n, B, p, j, counted[kr]);
+                    if (span_sees(s, kr) != want) fail("task row span", r.n, B, p, j, 0);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
 
 int main(int argc, char** argv) {
@@ -179,6 +255,9 @@ int main(int argc, char** argv) {
             check_backward(c, rnd(0, 1) ? 128 : 64);
             ++checked;
         }
+        // a task list over packed sequences
+        check_tasks(tile_rows);
+        ++checked;
         // a block group (whole blocks), ascending list
         {
             const int nb = rnd(1, 12), Bg = rnd(1, 24), ng = nb * Bg;

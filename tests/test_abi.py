@@ -115,6 +115,66 @@ def test_forward_rejects_bad_arguments(lib):
     assert lib.bdlm_last_launch_count() == 0
 
 
+def _tasks_call(lib, tasks, n_slots=2, L=256, block=16, heads=4, kv_heads=2, head_dim=128, o_dtype=0,
+                ws=256 * 1024, ws_bytes=1 << 30, q=256):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    arr = bd._task_array(tasks)
+    return lib.bdlm_attn_fwd_tasks(q, 512, 768, 1024, 2048, L, block, heads, kv_heads, head_dim, 0.0, arr,
+                                   len(tasks), n_slots, o_dtype, ws, ws_bytes, None)
+
+
+def test_task_list_rejects_bad_tasks(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    T = bd.Task
+    INVALID, UNSUP, WS = 1, 2, 3
+    ok = [T(0, 64, 0, 128, 0, 64, 0), T(128, 64, 0, 128, 64, 128, 1)]
+    assert _tasks_call(lib, ok, ws=None) == WS          # well-formed up to the missing workspace
+    assert _tasks_call(lib, ok, ws_bytes=64) == WS
+    assert _tasks_call(lib, ok, q=None) == INVALID
+    assert _tasks_call(lib, ok, q=17) == INVALID         # misaligned
+    assert _tasks_call(lib, ok, head_dim=96) == UNSUP
+    assert _tasks_call(lib, ok, n_slots=1) == INVALID    # slot 1 outside one slot
+    assert _tasks_call(lib, ok, o_dtype=5) == INVALID
+    assert _tasks_call(lib, []) == INVALID
+    bad = [
+        T(-1, 64, 0, 128, 0, 64),       # sequence before row 0
+        T(200, 64, 0, 128, 0, 64),      # sequence past L
+        T(0, 0, 0, 1, 0, 1),            # empty sequence
+        T(0, 64, 10, 10, 0, 64),        # empty row range
+        T(0, 64, 0, 129, 0, 64),        # rows past 2n
+        T(0, 64, 0, 128, 64, 64),       # empty key window
+        T(0, 64, 0, 128, 0, 129),       # keys past 2n
+        T(0, 64, 0, 128, 0, 64, -1),    # negative slot
+    ]
+    for t in bad:
+        assert _tasks_call(lib, [t]) == INVALID, t
+    # two tasks of one slot on overlapping rows; disjoint rows or other slots are fine
+    assert _tasks_call(lib, [T(0, 64, 0, 70, 0, 64), T(0, 64, 60, 128, 64, 128)]) == INVALID
+    assert _tasks_call(lib, [T(0, 64, 0, 60, 0, 64), T(0, 64, 60, 128, 64, 128)], ws=None) == WS
+    assert _tasks_call(lib, [T(0, 64, 0, 70, 0, 64, 0), T(0, 64, 60, 128, 64, 128, 1)], ws=None) == WS
+    assert _tasks_call(lib, [T(0, 64, 0, 100, 0, 64), T(64, 32, 0, 64, 0, 64)]) == INVALID  # rows 64..99 of both
+    # the reserved field must be 0
+    arr = bd._task_array(ok)
+    arr[0].reserved = 1
+    assert lib.bdlm_attn_fwd_tasks(256, 512, 768, 1024, 2048, 256, 16, 4, 2, 128, 0.0, arr, 2, 2, 0, 256 * 1024,
+                                   1 << 30, None) == INVALID
+    assert lib.bdlm_last_launch_count() == 0
+
+
+def test_task_list_workspace_size(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    T = bd.Task
+    one = bd.bdlm_attn_fwd_tasks_workspace_bytes([T(0, 1000, 0, 2000, 0, 10)])
+    # 2000 query rows split at n = 1000 give 8 + 8 tiles of 128 rows
+    many = bd.bdlm_attn_fwd_tasks_workspace_bytes([T(0, 1000, 0, 2000, 0, 10)] * 100)
+    assert 0 < one < many
+    assert bd.bdlm_attn_fwd_tasks_workspace_bytes([T(0, 10, 5, 5, 0, 10)]) == 0   # empty row range
+    assert bd.bdlm_attn_fwd_tasks_workspace_bytes([]) == 0
+
+
 def test_selftest_rejects_a_missing_workspace(lib):
     assert lib.bdlm_selftest_timeout(None, 256, 1000000, None) == 3   # BDLM_ERR_WORKSPACE
     assert lib.bdlm_selftest_timeout(256, 16, 1000000, None) == 3     # smaller than the header

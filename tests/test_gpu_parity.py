@@ -483,3 +483,91 @@ def test_mid_workload(bd):
     check_o(host(o)[rows], rs["o"][rows], "sampled o")
     check_lse(host(lse)[:, rows], rs["lse"][:, rows], "sampled lse")
     check_grad(host(dq)[rows], rs["dq"][rows], "sampled dq")
+
+
+# token-level task lists: one launch over tasks of several packed sequences
+TASK_CASES = [
+    # sequence clean lengths, block, H, Hk, d, o dtype
+    ((300, 200), 32, 4, 2, 128, torch.bfloat16),
+    ((300, 200), 32, 4, 2, 128, torch.float32),
+    ((129, 70, 256), 48, 2, 1, 128, torch.bfloat16),  # B divides none of them
+    ((150, 64), 16, 4, 4, 64, torch.float32),
+]
+
+
+def _task_grid(bd, starts, ns, rng):
+    """Per sequence: its rows cut into 3 ranges and its keys into 3 windows;
+    task (range, window w) writes slot w. Plus one task per sequence into
+    slot 3 on a random row range and key window."""
+    tasks = []
+    for s0, n in zip(starts, ns):
+        rc = [0, int(rng.integers(1, n)), int(rng.integers(n, 2 * n)), 2 * n]
+        kc = [0, int(rng.integers(1, n)), int(rng.integers(n, 2 * n)), 2 * n]
+        for qa, qb in zip(rc[:-1], rc[1:]):
+            for w, (ka, kb) in enumerate(zip(kc[:-1], kc[1:])):
+                tasks.append(bd.Task(s0, n, qa, qb, ka, kb, w))
+        qa = int(rng.integers(0, 2 * n - 1))
+        ka = int(rng.integers(0, 2 * n - 1))
+        tasks.append(bd.Task(s0, n, qa, int(rng.integers(qa + 1, 2 * n + 1)), ka, int(rng.integers(ka + 1, 2 * n + 1)), 3))
+    rng.shuffle(tasks)
+    return tasks
+
+
+@pytest.mark.parametrize("ns,block,H,Hk,d,odt", TASK_CASES)
+def test_task_list_forward(bd, ns, block, H, Hk, d, odt):
+    L = 2 * sum(ns)
+    starts = [int(s) for s in np.cumsum([0] + [2 * n for n in ns[:-1]])]
+    w, x = gen(ns[0], block, H, Hk, d, seed=31 + L, L=L)
+    tasks = _task_grid(bd, starts, ns, np.random.default_rng(L))
+    S = 4
+    # sentinels in the rows no task of a slot covers must survive
+    o = torch.full((S, L, H, d), 7.0, dtype=odt, device="cuda")
+    lse = torch.full((S, H, L), 3.0, dtype=torch.float32, device="cuda")
+    bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, block, tasks, S, out=o, lse=lse)
+    torch.cuda.synchronize()
+    ref = [dict(seq_start=t.seq_start, n=t.n, q_lo=t.q_lo, q_hi=t.q_hi, key_lo=t.key_lo, key_hi=t.key_hi,
+                slot=t.slot) for t in tasks]
+    ro, rl = oracle.task_attention(host(x.q), host(x.k), host(x.v), block, w.scale, ref, S)
+    go, gl = host(o), host(lse)
+    for s in range(S):
+        cov = ~np.isnan(rl[s, 0])
+        check_o(go[s][cov], ro[s][cov], f"slot {s} o")
+        check_lse(gl[s][:, cov], rl[s][:, cov], f"slot {s} lse")
+        assert np.all(go[s][~cov] == 7.0) and np.all(gl[s][:, ~cov] == 3.0), f"slot {s}: uncovered rows written"
+    # the slots 0-2 of each row split its keys: merged, they give the sequence's attention
+    om, lm = bd.bdlm_lse_merge([o[s] for s in range(3)], [lse[s] for s in range(3)])
+    torch.cuda.synchronize()
+    full = oracle.bdlm_attention(host(x.q), host(x.k), host(x.v), block, w.scale,
+                                 cu_seqlens=np.array(starts + [L], dtype=np.int64))
+    check_o(host(om), full["o"], "merged o")
+    check_lse(host(lm), full["lse"], "merged lse")
+
+
+def test_task_list_equals_window_calls(bd):
+    # the 8 clean shards + local corrupted keys of one sequence as one task
+    # list give the same bits as 9 key-window calls (same tiles, same order
+    # of arithmetic within a tile)
+    n, block, H, Hk, d = 1024, 32, 8, 2, 128
+    w, x = gen(n, block, H, Hk, d, seed=77)
+    cuts = [i * n // 8 for i in range(9)] + [2 * n]
+    tasks = [bd.Task(0, n, 0, 2 * n, a, b, i) for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:]))]
+    o, lse = bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, block, tasks, len(tasks))
+    assert bd.bdlm_last_launch_count() == 3  # upload, prologue, attention
+    for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        ow, lw = bd.bdlm_attn_fwd(x.q, x.k[a:b].contiguous(), x.v[a:b].contiguous(), block,
+                                  part=bd.Partial.window(a, b))
+        torch.cuda.synchronize()
+        assert torch.equal(o[i], ow), f"window {i}: o differs"
+        assert torch.equal(lse[i], lw), f"window {i}: lse differs"
+
+
+def test_task_list_rows_that_see_no_key(bd):
+    # clean rows against corrupted keys: o = 0, lse = -inf
+    n, block, H, Hk, d = 200, 16, 2, 1, 128
+    w, x = gen(n, block, H, Hk, d, seed=78)
+    o, lse = bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, block, [bd.Task(0, n, 0, n, n, 2 * n, 0)], 1,
+                                    out=torch.full((1, 2 * n, H, d), 5.0, dtype=torch.bfloat16, device="cuda"),
+                                    lse=torch.full((1, H, 2 * n), 5.0, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(o[0, :n] == 0) and torch.all(torch.isneginf(lse[0, :, :n]))
+    assert torch.all(o[0, n:] == 5.0) and torch.all(lse[0, :, n:] == 5.0)
