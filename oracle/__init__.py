@@ -17,5 +17,6 @@ from .bdlm_oracle import (  # noqa: F401
     mask_rows,
     partial_attention,
     task_attention,
+    task_attention_bwd,
     valid_pairs,
 )

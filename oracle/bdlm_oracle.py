@@ -327,6 +327,40 @@ def task_attention(q, k, v, block, scale, tasks, n_slots, o=None, lse=None):
     return o, lse
 
 
+def task_attention_bwd(q, k, v, o_full, lse_full, do, block, scale, tasks, n_slots):
+    """Backward of a task list, each task taken with the FULL softmax of its
+    rows (o_full [L, H, d], lse_full [H, L]: the merge over every key a row
+    sees), as in the sharded backward.
+
+    Returns dq [L, H, d], the sum of every task's dq share (0 on rows no task
+    covers), and dk, dv [S, L, Hk, d]: task t writes the gradients of its
+    window's keys from its rows into slot t (rows of k no task of a slot
+    covers stay NaN). Summed over a partition of every sequence's rows x keys
+    (with the tasks of one row range in one slot), dq, and dk, dv summed over
+    the slots, are the unsharded gradients.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    L, H, d = q.shape
+    Hk = k.shape[1]
+    dq = np.zeros((L, H, d))
+    dk = np.full((n_slots, L, Hk, d), np.nan)
+    dv = np.full((n_slots, L, Hk, d), np.nan)
+    for t in tasks:
+        s0, n = t["seq_start"], t["n"]
+        qa, qb = s0 + t["q_lo"], s0 + t["q_hi"]
+        ka, kb = s0 + t["key_lo"], s0 + t["key_hi"]
+        r = partial_attention(q[qa:qb], k[ka:kb], v[ka:kb], n, block, t["key_lo"], t["key_hi"], scale,
+                              do=do[qa:qb], o_full=o_full[qa:qb], lse_full=lse_full[:, qa:qb],
+                              q_lo=t["q_lo"], q_hi=t["q_hi"])
+        dq[qa:qb] += r["dq"]
+        dk[t["slot"], ka:kb] = r["dk"]
+        dv[t["slot"], ka:kb] = r["dv"]
+    return dq, dk, dv
+
+
 def valid_pairs(n, block):
     """Closed form of the mask's population per head for one sequence.
     With n = nb B + r: the clean rows of a full block b see (b+1)B keys, the

@@ -329,6 +329,45 @@ def test_task_list_over_packed_sequences():
     assert np.isnan(o2[0]).all() and np.isnan(o2[1, :s0]).all() and np.isnan(o2[1, s0 + n:]).all()
 
 
+def test_task_list_backward_over_packed_sequences():
+    # The backward of a task grid over two packed ragged sequences, each task
+    # with the full softmax of its rows: dq summed over the tasks and dk, dv
+    # summed over the slots (one slot per row range) give each sequence's
+    # unsharded gradients.
+    H, Hk, d, block = 4, 2, 8, 4
+    scale = 0.35
+    ns = [11, 18]
+    rows = 2 * sum(ns)
+    rng = np.random.default_rng(83)
+    q = rng.standard_normal((rows, H, d))
+    k = rng.standard_normal((rows, Hk, d))
+    v = rng.standard_normal((rows, Hk, d))
+    do = rng.standard_normal((rows, H, d))
+    starts = [0, 2 * ns[0]]
+    full_o = np.zeros((rows, H, d))
+    full_lse = np.zeros((H, rows))
+    alone = []
+    for s0, n in zip(starts, ns):
+        sl = slice(s0, s0 + 2 * n)
+        a = oracle.dense_bdlm_attention(q[sl], k[sl], v[sl], n, block, scale, do=do[sl])
+        full_o[sl], full_lse[:, sl] = a["o"], a["lse"]
+        alone.append(a)
+    tasks = []
+    for s0, n in zip(starts, ns):
+        row_cuts = [0, 6, n + 1, 2 * n]
+        key_cuts = [0, n - 2, n + 3, 2 * n]
+        for r, (qa, qb) in enumerate(zip(row_cuts[:-1], row_cuts[1:])):
+            for ka, kb in zip(key_cuts[:-1], key_cuts[1:]):
+                tasks.append(dict(seq_start=s0, n=n, q_lo=qa, q_hi=qb, key_lo=ka, key_hi=kb, slot=r))
+    dq, dk, dv = oracle.task_attention_bwd(q, k, v, full_o, full_lse, do, block, scale, tasks, 3)
+    assert not np.isnan(dk).any() and not np.isnan(dv).any()
+    for (s0, n), a in zip(zip(starts, ns), alone):
+        sl = slice(s0, s0 + 2 * n)
+        np.testing.assert_allclose(dq[sl], a["dq"], atol=1e-12)
+        np.testing.assert_allclose(dk[:, sl].sum(axis=0), a["dk"], atol=1e-12)
+        np.testing.assert_allclose(dv[:, sl].sum(axis=0), a["dv"], atol=1e-12)
+
+
 def test_merge_special_cases():
     rng = np.random.default_rng(70)
     R, H, d = 5, 2, 3
