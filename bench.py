@@ -303,27 +303,41 @@ class Step:
 
     def time_task_list(self, reps=3):
         """The same partial forwards as one task list (one attention launch
-        over all windows, into the same partial buffers; not part of the timed
-        step). Returns the median ms of `reps` runs after one warm-up (None
-        for packed documents)."""
+        over all windows, into the same partial buffers), and the backward of
+        the same windows as one task list (each window's keys complete, dq
+        summed over the windows: the full backward, key window by key window);
+        not part of the timed step. Returns the median ms of `reps` runs after
+        one warm-up of each (None, None for packed documents)."""
         bd, w, x = self.bd, self.w, self.x
         if not self.windows:
-            return None
+            return None, None
+        bwd_tasks = [bd.Task(0, w.n, 0, 2 * w.n, lo, hi, 0) for lo, hi in self.windows]
+        L, H, d = x.q.shape
+        ws_b = torch.empty(bd.bdlm_attn_bwd_tasks_workspace_bytes(bwd_tasks, L, H, d), dtype=torch.uint8,
+                           device=x.q.device)
 
-        def run():
+        def fwd():
             bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, w.block, self.tasks, len(self.tasks), out=self.parts_all,
                                    lse=self.plse_all, workspace=self.ws_t)
 
-        run()
-        times = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            run()
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
-        return statistics.median(times)
+        def bwd():
+            bd.bdlm_attn_bwd_tasks(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, bwd_tasks, 1, dq=self.dq,
+                                   dk=self.dk.unsqueeze(0), dv=self.dv.unsqueeze(0), workspace=ws_b)
+
+        out = []
+        for f in (fwd, bwd):
+            f()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                f()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            out.append(statistics.median(times))
+        del ws_b
+        return out[0], out[1]
 
     def time_running_merge(self, reps=2):
         """The same windows merged by the forward's epilogue into a running
@@ -439,12 +453,13 @@ def run_cuda(args, rank, world, local):
     achieved = f_bwd / (bwd_mean_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     run_ms = step.time_running_merge()
-    task_ms = step.time_task_list()
+    task_ms, task_bwd_ms = step.time_task_list()
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms)
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms,
+            task_bwd_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -531,7 +546,7 @@ def l2_note(x):
 
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms):
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms, task_bwd_ms):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -561,6 +576,8 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "fwd_running_merge_tflops": f_fwd / (run_ms / 1e3) / 1e12 if run_ms else None,
             "fwd_task_list_ms": task_ms,
             "fwd_task_list_tflops": f_fwd / (task_ms / 1e3) / 1e12 if task_ms else None,
+            "bwd_task_list_ms": task_bwd_ms,
+            "bwd_task_list_tflops": f_bwd / (task_bwd_ms / 1e3) / 1e12 if task_bwd_ms else None,
             "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
             # the forward's secondary bound: one exponential per valid (row, key) pair and head
             "fwd_exp_per_s": f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3),

@@ -11,6 +11,7 @@ The C functions are declared in include/bdlm.h; the Python names are the same:
   bdlm_lse_merge(partials, lses) -> (o, lse)
   bdlm_attn_fwd_tasks(q, k, v, block, tasks, n_slots) -> (o [S,L,H,d], lse [S,H,L])
                                     a token-level task list in one launch
+  bdlm_attn_bwd_tasks(q, k, v, o, lse, dO, block, tasks, n_slots) -> (dq, dk [S,L,Hk,d], dv)
   bdlm_attn_fwd_noalloc(...)        forward without a caller workspace
   bdlm_selftest_timeout(workspace)  device wait-timeout self-test
 Restrictions of a call (see Partial):
@@ -33,7 +34,8 @@ import torch
 from .build import LIB
 
 __all__ = [
-    "BDLMError", "Partial", "Task", "bdlm_attn_fwd", "bdlm_attn_fwd_tasks", "bdlm_attn_fwd_tasks_workspace_bytes", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
+    "BDLMError", "Partial", "Task", "bdlm_attn_fwd", "bdlm_attn_fwd_tasks", "bdlm_attn_fwd_tasks_workspace_bytes",
+    "bdlm_attn_bwd_tasks", "bdlm_attn_bwd_tasks_workspace_bytes", "bdlm_attn_fwd_noalloc", "bdlm_attn_bwd", "bdlm_lse_merge", "bdlm_read_error",
     "bdlm_attn_fwd_workspace_bytes", "bdlm_attn_bwd_workspace_bytes", "bdlm_last_launch_count",
     "bdlm_selftest_timeout", "load_library", "EXPORTED_SYMBOLS",
 ]
@@ -48,6 +50,7 @@ EXPORTED_SYMBOLS = (
     "bdlm_lse_merge", "bdlm_read_error", "bdlm_status_string", "bdlm_last_launch_count",
     "bdlm_attn_fwd_noalloc",
     "bdlm_attn_fwd_tasks_workspace_bytes", "bdlm_attn_fwd_tasks",
+    "bdlm_attn_bwd_tasks_workspace_bytes", "bdlm_attn_bwd_tasks",
     "bdlm_selftest_timeout",
 )
 
@@ -174,6 +177,11 @@ def load_library() -> ctypes.CDLL:
     lib.bdlm_attn_fwd_tasks.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                         ctypes.POINTER(_CTask), i32, i32, i32, vp, sz, vp]
     lib.bdlm_attn_fwd_tasks.restype = ctypes.c_int
+    lib.bdlm_attn_bwd_tasks_workspace_bytes.argtypes = [ctypes.POINTER(_CTask), i32, i64, i32, i32]
+    lib.bdlm_attn_bwd_tasks_workspace_bytes.restype = sz
+    lib.bdlm_attn_bwd_tasks.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
+                                        ctypes.POINTER(_CTask), i32, i32, vp, sz, vp]
+    lib.bdlm_attn_bwd_tasks.restype = ctypes.c_int
     lib.bdlm_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
     lib.bdlm_selftest_timeout.restype = ctypes.c_int
     _lib = lib
@@ -311,6 +319,47 @@ def bdlm_attn_fwd_tasks(q, k, v, block: int, tasks: Sequence[Task], n_slots: int
                                  workspace.numel(), _stream(stream))
     _check(st, "bdlm_attn_fwd_tasks")
     return out, lse
+
+
+def bdlm_attn_bwd_tasks_workspace_bytes(tasks: Sequence[Task], L: int, heads: int, head_dim: int) -> int:
+    return int(load_library().bdlm_attn_bwd_tasks_workspace_bytes(_task_array(tasks), len(tasks), L, heads,
+                                                                  head_dim))
+
+
+def bdlm_attn_bwd_tasks(q, k, v, o, lse, dO, block: int, tasks: Sequence[Task], n_slots: int, *,
+                        softmax_scale: float = 0.0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Every task's backward in one launch, each with the full softmax of its
+    rows (o, lse: the merged forward results). Returns (dq [L,H,d]: the sum of
+    the tasks' dq shares; dk, dv [n_slots,L,Hk,d]: task t's window keys in
+    slot t.slot; keys no task of a slot covers keep what `dk` / `dv` held,
+    zeros for fresh outputs)."""
+    lib = load_library()
+    for nm, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        _bf16_cuda(nm, t)
+    L, H, d = q.shape
+    Hk = k.shape[1]
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.zeros((n_slots, L, Hk, d), dtype=torch.bfloat16, device=q.device)
+    if dv is None:
+        dv = torch.zeros((n_slots, L, Hk, d), dtype=torch.bfloat16, device=q.device)
+    _bf16_cuda("dq", dq)
+    for nm, t in (("dk", dk), ("dv", dv)):
+        _bf16_cuda(nm, t)
+        if tuple(t.shape) != (n_slots, L, Hk, d):
+            raise ValueError(f"{nm} must be [n_slots, L, Hk, d]")
+    if tuple(lse.shape) != (H, L) or lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [H, L]")
+    arr = _task_array(tasks)
+    if workspace is None:
+        ws_bytes = lib.bdlm_attn_bwd_tasks_workspace_bytes(arr, len(tasks), L, H, d)
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.bdlm_attn_bwd_tasks(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+                                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), L, block, H, Hk, d, softmax_scale, arr,
+                                 len(tasks), n_slots, workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(st, "bdlm_attn_bwd_tasks")
+    return dq, dk, dv
 
 
 def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=None,

@@ -53,8 +53,8 @@ size_t sched_bytes_mt(long long mt) {
 size_t sched_bytes(long long L, int n_docs) { return sched_bytes_mt(max_tiles_for(L, n_docs)); }
 
 // Workspace carve-up for at most mt tiles; then, for the backward, D and the
-// dq accumulator, or, for a task list, its n_tasks records.
-WsCarve carve_mt(void* ws, long long mt, long long L, int H, bool bwd, int n_tasks) {
+// dq accumulator; then, for a task list, its n_tasks records.
+WsCarve carve_mt(void* ws, long long mt, long long L, int H, int d, bool bwd, int n_tasks) {
     WsCarve c{};
     uint8_t* p = static_cast<uint8_t*>(ws);
     c.hdr = reinterpret_cast<WsHeader*>(p);
@@ -74,34 +74,69 @@ WsCarve carve_mt(void* ws, long long mt, long long L, int H, bool bwd, int n_tas
         c.D = reinterpret_cast<float*>(p);
         p += round_up((size_t)L * H * sizeof(float), 256);
         c.dqacc = reinterpret_cast<float*>(p);
+        p += round_up((size_t)L * H * d * sizeof(float), 256);
     }
     if (n_tasks > 0) c.tasks = reinterpret_cast<TaskRec*>(p);
     return c;
 }
 
 WsCarve carve(void* ws, long long L, int n_docs, int H, int d, bool bwd) {
-    (void)d;
-    return carve_mt(ws, max_tiles_for(L, n_docs), L, H, bwd, 0);
+    return carve_mt(ws, max_tiles_for(L, n_docs), L, H, d, bwd, 0);
 }
 
 constexpr int kMaxTasks = 65536;
 constexpr int kMaxSlots = 1024;
 
-// Forward tiles of one task (its query positions in two runs split at n).
-long long task_tiles(const bdlm_task& t) {
-    auto run = [](long long lo, long long hi) { return hi > lo ? (hi - lo + kFwdTileRows - 1) / kFwdTileRows : 0; };
-    return run(t.q_lo, std::min(t.q_hi, t.n)) + run(std::max(t.q_lo, t.n), t.q_hi);
+// Tiles of one task: forward - its query positions in 128-row tiles;
+// backward - its key positions in 64-key tiles (the smaller backward tile);
+// each in two runs split at n.
+long long task_tiles(const bdlm_task& t, bool bwd) {
+    const long long rows = bwd ? kBwdKeyTile : kFwdTileRows;
+    auto run = [rows](long long lo, long long hi) { return hi > lo ? (hi - lo + rows - 1) / rows : 0; };
+    const long long lo = bwd ? t.key_lo : t.q_lo, hi = bwd ? t.key_hi : t.q_hi;
+    const long long n = t.n;
+    return run(lo, std::min(hi, n)) + run(std::max(lo, n), hi);
 }
 
 // Tile bound of a task list; -1 for an empty list or a task of empty size.
-long long tasks_max_tiles(const bdlm_task* tasks, int n_tasks) {
+long long tasks_max_tiles(const bdlm_task* tasks, int n_tasks, bool bwd) {
     if (!tasks || n_tasks < 1 || n_tasks > kMaxTasks) return -1;
     long long mt = 4;
     for (int i = 0; i < n_tasks; ++i) {
-        if (tasks[i].n <= 0 || tasks[i].q_hi <= tasks[i].q_lo || tasks[i].q_hi - tasks[i].q_lo > kMaxRows) return -1;
-        mt += task_tiles(tasks[i]);
+        const bdlm_task& t = tasks[i];
+        if (t.n <= 0 || t.n > kMaxRows || t.q_hi <= t.q_lo || t.q_hi - t.q_lo > kMaxRows) return -1;
+        if (bwd && (t.key_hi <= t.key_lo || t.key_hi - t.key_lo > kMaxRows)) return -1;
+        mt += task_tiles(t, bwd);
     }
     return mt;
+}
+
+// Host checks of a task list (every task inside its sequence, every sequence
+// inside [0, L); the tasks of one slot write disjoint rows of q (forward) or
+// of k (backward)); fills the device records and the longest clean length.
+int check_tasks(const bdlm_task* tasks, int n_tasks, long long L, int n_slots, bool bwd, std::vector<TaskRec>* rec,
+                long long* max_n) {
+    if (!tasks || n_tasks < 1 || n_tasks > kMaxTasks || n_slots < 1 || n_slots > kMaxSlots) return BDLM_ERR_INVALID_ARG;
+    rec->assign((size_t)n_tasks, TaskRec{});
+    *max_n = 1;
+    for (int i = 0; i < n_tasks; ++i) {
+        const bdlm_task& t = tasks[i];
+        if (t.reserved != 0 || t.slot < 0 || t.slot >= n_slots) return BDLM_ERR_INVALID_ARG;
+        if (t.seq_start < 0 || t.n < 1 || t.n > L / 2 || t.seq_start > L - 2 * t.n) return BDLM_ERR_INVALID_ARG;
+        if (t.q_lo < 0 || t.q_hi <= t.q_lo || t.q_hi > 2 * t.n) return BDLM_ERR_INVALID_ARG;
+        if (t.key_lo < 0 || t.key_hi <= t.key_lo || t.key_hi > 2 * t.n) return BDLM_ERR_INVALID_ARG;
+        (*rec)[i] = TaskRec{(int)t.seq_start, (int)t.n, (int)t.key_lo, (int)t.key_hi, (int)t.q_lo, (int)t.q_hi, t.slot, 0};
+        *max_n = std::max(*max_n, (long long)t.n);
+    }
+    std::vector<int> ord((size_t)n_tasks);
+    for (int i = 0; i < n_tasks; ++i) ord[i] = i;
+    const std::vector<TaskRec>& r = *rec;
+    auto lo = [&](int i) { return (long long)r[i].seq_start + (bwd ? r[i].kw_lo : r[i].q_lo); };
+    auto hi = [&](int i) { return (long long)r[i].seq_start + (bwd ? r[i].kw_hi : r[i].q_hi); };
+    std::sort(ord.begin(), ord.end(), [&](int a, int b) { return r[a].slot != r[b].slot ? r[a].slot < r[b].slot : lo(a) < lo(b); });
+    for (int i = 1; i < n_tasks; ++i)
+        if (r[ord[i - 1]].slot == r[ord[i]].slot && lo(ord[i]) < hi(ord[i - 1])) return BDLM_ERR_INVALID_ARG;
+    return BDLM_OK;
 }
 
 struct Common {
@@ -246,9 +281,19 @@ int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
 }
 
 size_t bdlm_attn_fwd_tasks_workspace_bytes(const bdlm_task* tasks, int32_t n_tasks) {
-    const long long mt = tasks_max_tiles(tasks, n_tasks);
+    const long long mt = tasks_max_tiles(tasks, n_tasks, false);
     if (mt < 0) return 0;
     return sched_bytes_mt(mt) + round_up((size_t)n_tasks * sizeof(TaskRec), 256);
+}
+
+size_t bdlm_attn_bwd_tasks_workspace_bytes(const bdlm_task* tasks, int32_t n_tasks, int64_t L, int32_t heads,
+                                           int32_t head_dim) {
+    const long long mt = tasks_max_tiles(tasks, n_tasks, true);
+    if (mt < 0 || L <= 0 || L > kMaxRows || heads <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    size_t b = sched_bytes_mt(mt);
+    b += round_up((size_t)L * heads * sizeof(float), 256);
+    b += round_up((size_t)L * heads * head_dim * sizeof(float), 256);
+    return b + round_up((size_t)n_tasks * sizeof(TaskRec), 256);
 }
 
 int bdlm_attn_fwd_tasks(const void* q, const void* k, const void* v, void* o, float* lse, int64_t L, int32_t block,
@@ -262,40 +307,17 @@ int bdlm_attn_fwd_tasks(const void* q, const void* k, const void* v, void* o, fl
     if (L <= 0 || L > kMaxRows || block <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads != 0)
         return BDLM_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return BDLM_ERR_UNSUPPORTED;
-    if (n_tasks < 1 || n_tasks > kMaxTasks || n_slots < 1 || n_slots > kMaxSlots) return BDLM_ERR_INVALID_ARG;
     if (o_dtype != BDLM_BF16 && o_dtype != BDLM_F32) return BDLM_ERR_INVALID_ARG;
-    // every task inside its sequence, every sequence inside [0, L)
-    std::vector<TaskRec> rec((size_t)n_tasks);
+    std::vector<TaskRec> rec;
     long long max_n = 1;
-    for (int i = 0; i < n_tasks; ++i) {
-        const bdlm_task& t = tasks[i];
-        if (t.reserved != 0 || t.slot < 0 || t.slot >= n_slots) return BDLM_ERR_INVALID_ARG;
-        if (t.seq_start < 0 || t.n < 1 || t.n > L / 2 || t.seq_start > L - 2 * t.n) return BDLM_ERR_INVALID_ARG;
-        if (t.q_lo < 0 || t.q_hi <= t.q_lo || t.q_hi > 2 * t.n) return BDLM_ERR_INVALID_ARG;
-        if (t.key_lo < 0 || t.key_hi <= t.key_lo || t.key_hi > 2 * t.n) return BDLM_ERR_INVALID_ARG;
-        rec[i] = TaskRec{(int)t.seq_start, (int)t.n, (int)t.key_lo, (int)t.key_hi, (int)t.q_lo, (int)t.q_hi, t.slot, 0};
-        max_n = std::max(max_n, (long long)t.n);
-    }
-    // the tasks of one slot write disjoint rows
-    {
-        std::vector<int> ord((size_t)n_tasks);
-        for (int i = 0; i < n_tasks; ++i) ord[i] = i;
-        auto row0 = [&](int i) { return (long long)rec[i].seq_start + rec[i].q_lo; };
-        std::sort(ord.begin(), ord.end(), [&](int a, int b) {
-            return rec[a].slot != rec[b].slot ? rec[a].slot < rec[b].slot : row0(a) < row0(b);
-        });
-        for (int i = 1; i < n_tasks; ++i) {
-            const TaskRec& p = rec[ord[i - 1]];
-            const TaskRec& c = rec[ord[i]];
-            if (p.slot == c.slot && row0(ord[i]) < (long long)p.seq_start + p.q_hi) return BDLM_ERR_INVALID_ARG;
-        }
-    }
+    const int st = check_tasks(tasks, n_tasks, L, n_slots, false, &rec, &max_n);
+    if (st != BDLM_OK) return st;
     if (!workspace || !aligned256(workspace)) return BDLM_ERR_WORKSPACE;
     if (workspace_bytes < bdlm_attn_fwd_tasks_workspace_bytes(tasks, n_tasks)) return BDLM_ERR_WORKSPACE;
     const int sms = num_sms();
     if (sms <= 0) return BDLM_ERR_CUDA;
 
-    WsCarve ws = carve_mt(workspace, tasks_max_tiles(tasks, n_tasks), L, heads, false, n_tasks);
+    WsCarve ws = carve_mt(workspace, tasks_max_tiles(tasks, n_tasks, false), L, heads, head_dim, false, n_tasks);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int launches = launch_task_upload(rec.data(), n_tasks, ws.tasks, s);
     Layout lay;
@@ -330,6 +352,72 @@ int bdlm_attn_fwd_tasks(const void* q, const void* k, const void* v, void* o, fl
     a.table = ws.table;
     a.hdr = ws.hdr;
     if (launch_fwd_tc(a, ws.ranges, sms, s, &launches) != cudaSuccess) return BDLM_ERR_CUDA;
+    g_launches = launches;
+    return BDLM_OK;
+}
+
+int bdlm_attn_bwd_tasks(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, int64_t L, int32_t block, int32_t heads, int32_t kv_heads,
+                        int32_t head_dim, float softmax_scale, const bdlm_task* tasks, int32_t n_tasks,
+                        int32_t n_slots, void* workspace, size_t workspace_bytes, bdlm_stream_t stream) {
+    g_launches = 0;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !tasks) return BDLM_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return BDLM_ERR_INVALID_ARG;
+    if (L <= 0 || L > kMaxRows || block <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads != 0)
+        return BDLM_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return BDLM_ERR_UNSUPPORTED;
+    std::vector<TaskRec> rec;
+    long long max_n = 1;
+    const int st = check_tasks(tasks, n_tasks, L, n_slots, true, &rec, &max_n);
+    if (st != BDLM_OK) return st;
+    if (!workspace || !aligned256(workspace)) return BDLM_ERR_WORKSPACE;
+    if (workspace_bytes < bdlm_attn_bwd_tasks_workspace_bytes(tasks, n_tasks, L, heads, head_dim))
+        return BDLM_ERR_WORKSPACE;
+    const int sms = num_sms();
+    if (sms <= 0) return BDLM_ERR_CUDA;
+
+    WsCarve ws = carve_mt(workspace, tasks_max_tiles(tasks, n_tasks, true), L, heads, head_dim, true, n_tasks);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int launches = launch_task_upload(rec.data(), n_tasks, ws.tasks, s);
+    Layout lay;
+    std::memset(&lay, 0, sizeof(lay));
+    lay.mode = MODE_TASKS;
+    lay.B = block;
+    lay.n = (int)max_n;  // the longest sequence bounds every tile's cost
+    lay.n_docs = 1;
+    lay.L = L;
+    lay.tasks = ws.tasks;
+    lay.n_tasks = n_tasks;
+    launch_enumerate(lay, head_dim == 128 ? kBwdTcKeyTile : kBwdKeyTile, kBwdQTile, 1, ws, s);
+    if (cudaGetLastError() != cudaSuccess) return BDLM_ERR_CUDA;
+    ++launches;
+
+    BwdArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.o = static_cast<const __nv_bfloat16*>(o);
+    a.lse = lse;
+    a.dO = static_cast<const __nv_bfloat16*>(dO);
+    a.dq = static_cast<__nv_bfloat16*>(dq);
+    a.dk = static_cast<__nv_bfloat16*>(dk);
+    a.dv = static_cast<__nv_bfloat16*>(dv);
+    a.Dsum = ws.D;
+    a.dqacc = ws.dqacc;
+    a.lay = lay;
+    a.H = heads;
+    a.Hk = kv_heads;
+    a.G = heads / kv_heads;
+    a.D = head_dim;
+    a.scale = pick_scale(softmax_scale, head_dim);
+    a.scale_log2 = a.scale * 1.4426950408889634f;
+    a.Lq = L;
+    a.Lk = L;
+    a.table = ws.table;
+    a.hdr = ws.hdr;
+    if (launch_bwd(a, sms, s, &launches) != cudaSuccess) return BDLM_ERR_CUDA;
     g_launches = launches;
     return BDLM_OK;
 }

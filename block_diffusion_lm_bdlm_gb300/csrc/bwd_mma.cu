@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
             const int h = kvh * G + hh;
             const int p0 = rem < na ? ra_lo + rem * BQ : rb_lo + (rem - na) * BQ;
             const int hi = rem < na ? ra_hi : rb_hi;
-            const Tile qt{kt.doc_start, n, p0, imin(BQ, hi - p0)};
+            const Tile qt{kt.doc_start, n, p0, imin(BQ, hi - p0), kt.task};
             const long long qr0 = q_row_of(a.lay, kt, p0);
             load_tile_async<D, BQ, NT>(sQ0 + buf * BQ * D * 2, a.q, qr0, qr0 + qt.nrows, q_stride, h);
             load_tile_async<D, BQ, NT>(sO0 + buf * BQ * D * 2, a.dO, qr0, qr0 + qt.nrows, q_stride, h);
@@ -279,13 +279,15 @@ __global__ void __launch_bounds__(NT, 2) bwd_mma_kernel(const BwdArgs a) {
         }
         cp_async_wait<0>();
 
-        // write dK (scaled) and dV for this warp's keys
+        // write dK (scaled) and dV for this warp's keys (dk, dv [slots, Lk,
+        // Hk, D]: a task list's tile writes its task's slot)
+        const long long kslot = a.lay.mode == MODE_TASKS ? (long long)ld_ro(&a.lay.tasks[kt.task].slot) * a.Lk : 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int kk = warp * 16 + g + 8 * i;
             if (kk < kv_rows) {
-                __nv_bfloat16* dkr = a.dk + (long long)(k0 + kk) * k_stride + (long long)kvh * D + 2 * tq;
-                __nv_bfloat16* dvr = a.dv + (long long)(k0 + kk) * k_stride + (long long)kvh * D + 2 * tq;
+                __nv_bfloat16* dkr = a.dk + (kslot + k0 + kk) * k_stride + (long long)kvh * D + 2 * tq;
+                __nv_bfloat16* dvr = a.dv + (kslot + k0 + kk) * k_stride + (long long)kvh * D + 2 * tq;
 #pragma unroll
                 for (int dn = 0; dn < D / 8; ++dn) {
                     *reinterpret_cast<uint32_t*>(dkr + dn * 8) =

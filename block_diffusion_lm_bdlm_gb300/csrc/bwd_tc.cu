@@ -429,7 +429,9 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
     const int kk = dl;
     const bool key_ok = kk < c.kv_rows;
     const bool seen = c.n_steps > 0;
-    const long long rowoff = (long long)(c.k0 + kk) * ((long long)a.Hk * D) + (long long)c.kvh * D;
+    // dk, dv [slots, Lk, Hk, D]: a task list's tile writes its task's slot
+    const int slot = a.lay.mode == MODE_TASKS ? ld_ro(&a.lay.tasks[c.kt.task].slot) : 0;
+    const long long rowoff = ((long long)slot * a.Lk + c.k0 + kk) * ((long long)a.Hk * D) + (long long)c.kvh * D;
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
         const uint32_t src = which == 0 ? TDK : TDV;

@@ -197,10 +197,10 @@ __host__ __device__ __forceinline__ bool rel_sees(const RelInterval& r, int e) {
 // ---------------------------------------------------------------------------
 // Key-major view (backward). A backward tile is a run of consecutive keys that
 // never straddles the clean/corrupted boundary. Tile.pos0 is the sequence
-// position of key 0 (full: document position; window: global position) or,
-// for a block group, its k row (clean keys [0, n), then the group's corrupted
-// rows). "Row positions" of the query side map to q rows as doc_start + p
-// (full), p (window: q holds the whole sequence) or the list row p (group).
+// position of key 0 (full and tasks: document position; window: global
+// position) or, for a block group, its k row (clean keys [0, n), then the
+// group's corrupted rows). "Row positions" of the query side map to q rows as
+// doc_start + p (full, tasks), p - q_lo (window) or the list row p (group).
 // ---------------------------------------------------------------------------
 
 // Number of list entries with block id <= b. The backward requires a strictly
@@ -256,12 +256,14 @@ __host__ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, con
         r.a_lo = n + ((t.pos0 - n) / B) * B;
         r.a_hi = imin(n + ((t.pos0 + t.nrows - 1 - n) / B + 1) * B, 2 * n);  // a last block may be short
     }
-    if (lay.mode == MODE_WINDOW) {  // only the call's query rows
-        r.a_lo = imax(r.a_lo, lay.q_lo);
-        r.a_hi = imin(r.a_hi, lay.q_hi);
+    if (lay.mode == MODE_WINDOW || lay.mode == MODE_TASKS) {  // only the call's (task's) query rows
+        const int qlo = lay.mode == MODE_WINDOW ? lay.q_lo : ld_ro(&lay.tasks[t.task].q_lo);
+        const int qhi = lay.mode == MODE_WINDOW ? lay.q_hi : ld_ro(&lay.tasks[t.task].q_hi);
+        r.a_lo = imax(r.a_lo, qlo);
+        r.a_hi = imin(r.a_hi, qhi);
         if (r.a_hi <= r.a_lo) { r.a_lo = 0; r.a_hi = 0; }
-        r.b_lo = imax(r.b_lo, lay.q_lo);
-        r.b_hi = imin(r.b_hi, lay.q_hi);
+        r.b_lo = imax(r.b_lo, qlo);
+        r.b_hi = imin(r.b_hi, qhi);
         if (r.b_hi <= r.b_lo) { r.b_lo = 0; r.b_hi = 0; }
     }
     return r;

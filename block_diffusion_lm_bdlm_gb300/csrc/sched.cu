@@ -151,16 +151,18 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         __syncthreads();
     } else if (lay.mode == MODE_TASKS) {
         // tasks in chunks of kThreads: scan the per-task tile counts (each
-        // task's query positions in two runs split at its clean/corrupted
-        // boundary), then let every thread fill tiles, finding its task by
-        // binary search over the chunk's tile offsets
+        // task's query positions (forward) or key positions (backward) in two
+        // runs split at its clean/corrupted boundary), then let every thread
+        // fill tiles, finding its task by binary search over the chunk's tile
+        // offsets
         for (int base = 0; base < lay.n_tasks; base += kThreads) {
             const int ti = base + tid;
             const int nt = imin(kThreads, lay.n_tasks - base);
             int cnt = 0;
             if (ti < lay.n_tasks) {
                 const TaskRec r = lay.tasks[ti];
-                cnt = run_tiles(r.q_lo, imin(r.q_hi, r.n), tile_rows) + run_tiles(imax(r.q_lo, r.n), r.q_hi, tile_rows);
+                const int lo = kind == 0 ? r.q_lo : r.kw_lo, hi = kind == 0 ? r.q_hi : r.kw_hi;
+                cnt = run_tiles(lo, imin(hi, r.n), tile_rows) + run_tiles(imax(lo, r.n), hi, tile_rows);
             }
             int total;
             const int off = block_exclusive_scan(cnt, &total, sbuf);
@@ -174,11 +176,12 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
                     if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
                 }
                 const TaskRec r = lay.tasks[base + lo];
+                const int a0 = kind == 0 ? r.q_lo : r.kw_lo, a1 = kind == 0 ? r.q_hi : r.kw_hi;
                 const int li = i - s_off[lo];
-                const int c_hi = imin(r.q_hi, r.n);
-                const int nc = run_tiles(r.q_lo, c_hi, tile_rows);
-                const int p0 = li < nc ? r.q_lo + li * tile_rows : imax(r.q_lo, r.n) + (li - nc) * tile_rows;
-                const int end = li < nc ? c_hi : r.q_hi;
+                const int c_hi = imin(a1, r.n);
+                const int nc = run_tiles(a0, c_hi, tile_rows);
+                const int p0 = li < nc ? a0 + li * tile_rows : imax(a0, r.n) + (li - nc) * tile_rows;
+                const int end = li < nc ? c_hi : a1;
                 const int idx = carry + i;
                 if (idx < max_tiles) tmp[idx] = Tile{r.seq_start, r.n, p0, imin(tile_rows, end - p0), base + lo};
             }

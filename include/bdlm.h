@@ -234,6 +234,42 @@ BDLM_API int bdlm_attn_fwd_tasks(const void* q, const void* k, const void* v, vo
                   float softmax_scale, const bdlm_task* tasks, int32_t n_tasks, int32_t n_slots,
                   int32_t o_dtype, void* workspace, size_t workspace_bytes, bdlm_stream_t stream);
 
+/* Workspace (bytes, 256-byte aligned) of a task-list backward over this HOST
+ * task array with L rows, H heads and head dim d; 0 if the list or a task is
+ * malformed as for bdlm_attn_fwd_tasks_workspace_bytes (or has an empty key
+ * window), or the sizes are unsupported. */
+BDLM_API size_t bdlm_attn_bwd_tasks_workspace_bytes(const bdlm_task* tasks, int32_t n_tasks, int64_t L,
+                  int32_t heads, int32_t head_dim);
+
+/*
+ * bdlm_attn_bwd_tasks - the backward of every task of a list, in one launch of
+ * the backward's main kernel (after the task upload and the prologue, and
+ * with the same preprocess and dq-convert kernels as bdlm_attn_bwd). Each
+ * task's backward is taken with the FULL softmax of its rows, as for a
+ * KEY_WINDOW backward: o and lse hold, for every row a task covers, the merge
+ * over all the keys the row sees (e.g. the bdlm_lse_merge of the forward's
+ * slots), and D = rowsum(dO * o).
+ *
+ *   q, o, dO   bf16 [L, H, d]; lse fp32 [H, L]; k, v bf16 [L, Hk, d].
+ *   dq         bf16 [L, H, d]: the sum over the tasks of each task's dq share
+ *              (its rows' gradient through its keys); 0 on rows no task covers.
+ *              Over tasks that split each row's keys, it is the full dq.
+ *   dk, dv     n_slots consecutive bf16 [L, Hk, d] arrays: task t writes the
+ *              gradients of its window's keys from its rows into slot t (zeros
+ *              for keys that none of its rows sees); keys that no task of a
+ *              slot covers are left as they were. Summed over the slots, the
+ *              tasks of a partition of every sequence's rows x keys give the
+ *              full dk, dv.
+ * Tasks of one slot must not share keys (they would write the same dk, dv
+ * rows): such a list returns BDLM_ERR_INVALID_ARG, as do the per-task checks
+ * of bdlm_attn_fwd_tasks. Tasks of one slot may share query rows.
+ */
+BDLM_API int bdlm_attn_bwd_tasks(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv,
+                  int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
+                  float softmax_scale, const bdlm_task* tasks, int32_t n_tasks, int32_t n_slots,
+                  void* workspace, size_t workspace_bytes, bdlm_stream_t stream);
+
 /*
  * Backward: given q, k, v, the forward's o and lse, and the upstream gradient
  * dO, writes dq [Lq, H, d], dk [Lk, Hk, d], dv [Lk, Hk, d] (bf16), the

@@ -215,6 +215,31 @@ void check_tasks(int tile_rows) {
                 }
             }
         }
+        // backward: key tiles over the task's window; the query rows of each
+        // key are exactly the task's rows that see it
+        const int key_rows_per_tile = rnd(0, 1) ? 128 : 64;
+        for (const Tile& t0 : tiles(r.kw_lo, r.kw_hi, r.n, key_rows_per_tile, r.n)) {
+            Tile t = t0;
+            t.doc_start = r.seq_start;
+            t.task = ti;
+            const KeyRows tr = key_tile_rows(lay, t);
+            const int k0 = key_row0(lay, t);
+            if (k0 != r.seq_start + t.pos0) fail("task key row", r.n, B, t.pos0, ti, k0);
+            if ((tr.a_hi > tr.a_lo && (tr.a_lo < r.q_lo || tr.a_hi > r.q_hi)) ||
+                (tr.b_hi > tr.b_lo && (tr.b_lo < r.q_lo || tr.b_hi > r.q_hi)))
+                fail("task tile rows outside the task", r.n, B, tr.a_lo, tr.a_hi, tr.b_hi);
+            for (int kk = 0; kk < t.nrows; ++kk) {
+                const int j = t.pos0 + kk;
+                const KeyRows kr = key_rows(lay, t, kk);
+                for (int p = 0; p < 2 * r.n; ++p) {
+                    const bool want = p >= r.q_lo && p < r.q_hi && visible(p, j, r.n, B);
+                    const bool in_tile = (p >= tr.a_lo && p < tr.a_hi) || (p >= tr.b_lo && p < tr.b_hi);
+                    const bool got = in_tile && ((p >= kr.a_lo && p < kr.a_hi) || (p >= kr.b_lo && p < kr.b_hi));
+                    if (got != want) fail("task rows of a key", r.n, B, p, j, (int)got);
+                    if (got && q_row_of(lay, t, p) != r.seq_start + p) fail("task bwd q row", r.n, B, p, j, 0);
+                }
+            }
+        }
     }
 }
 

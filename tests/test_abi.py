@@ -163,6 +163,34 @@ def test_task_list_rejects_bad_tasks(lib):
     assert lib.bdlm_last_launch_count() == 0
 
 
+def test_task_list_backward_rejects_bad_tasks(lib):
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    T = bd.Task
+    INVALID, UNSUP, WS = 1, 2, 3
+
+    def call(tasks, n_slots=2, ws=256 * 1024, head_dim=128, dq=4096):
+        arr = bd._task_array(tasks)
+        return lib.bdlm_attn_bwd_tasks(256, 512, 768, 1024, 2048, 3072, dq, 8192, 16384, 256, 16, 4, 2, head_dim,
+                                       0.0, arr, len(tasks), n_slots, ws, 1 << 30, None)
+
+    ok = [T(0, 64, 0, 128, 0, 64, 0), T(0, 64, 0, 128, 64, 128, 0)]   # one slot, disjoint keys, shared rows
+    assert call(ok, ws=None) == WS
+    assert call(ok, dq=None) == INVALID
+    assert call(ok, dq=4100) == INVALID        # misaligned
+    assert call(ok, head_dim=96) == UNSUP
+    assert call([]) == INVALID
+    # two tasks of one slot on overlapping keys; other slots are fine
+    assert call([T(0, 64, 0, 64, 0, 70), T(0, 64, 64, 128, 60, 128)]) == INVALID
+    assert call([T(0, 64, 0, 64, 0, 70, 0), T(0, 64, 64, 128, 60, 128, 1)], ws=None) == WS
+    assert call([T(0, 64, 0, 128, 0, 129)]) == INVALID   # keys past 2n
+    assert lib.bdlm_last_launch_count() == 0
+    w = bd.bdlm_attn_bwd_tasks_workspace_bytes(ok, 256, 4, 128)
+    assert w > bd.bdlm_attn_fwd_tasks_workspace_bytes(ok)  # holds D and the fp32 dq accumulator
+    assert w >= 256 * 4 * 128 * 4 + 256 * 4 * 4
+    assert bd.bdlm_attn_bwd_tasks_workspace_bytes(ok, 256, 4, 96) == 0
+
+
 def test_task_list_workspace_size(lib):
     import block_diffusion_lm_bdlm_gb300 as bd
 

@@ -571,3 +571,53 @@ def test_task_list_rows_that_see_no_key(bd):
     torch.cuda.synchronize()
     assert torch.all(o[0, :n] == 0) and torch.all(torch.isneginf(lse[0, :, :n]))
     assert torch.all(o[0, n:] == 5.0) and torch.all(lse[0, :, n:] == 5.0)
+
+
+TASK_BWD_CASES = [
+    # sequence clean lengths, block, H, Hk, d
+    ((300, 200), 32, 4, 2, 128),
+    ((129, 70, 256), 48, 2, 1, 128),  # B divides none of them
+    ((150, 64), 16, 4, 4, 64),        # warp-level backward
+]
+
+
+@pytest.mark.parametrize("ns,block,H,Hk,d", TASK_BWD_CASES)
+def test_task_list_backward(bd, ns, block, H, Hk, d):
+    # per sequence: rows cut into 3 ranges (slot = range), keys into 3
+    # windows; plus slot 3 holding one task per sequence on part of its keys
+    L = 2 * sum(ns)
+    starts = [int(s) for s in np.cumsum([0] + [2 * n for n in ns[:-1]])]
+    w, x = gen(ns[0], block, H, Hk, d, seed=41 + L, L=L)
+    rng = np.random.default_rng(L + 1)
+    tasks = []
+    for s0, n in zip(starts, ns):
+        rc = [0, int(rng.integers(1, n)), int(rng.integers(n, 2 * n)), 2 * n]
+        kc = [0, int(rng.integers(1, n)), int(rng.integers(n, 2 * n)), 2 * n]
+        for r, (qa, qb) in enumerate(zip(rc[:-1], rc[1:])):
+            for ka, kb in zip(kc[:-1], kc[1:]):
+                tasks.append(bd.Task(s0, n, qa, qb, ka, kb, r))
+        ka = int(rng.integers(0, 2 * n - 1))
+        tasks.append(bd.Task(s0, n, 0, 2 * n, ka, int(rng.integers(ka + 1, 2 * n + 1)), 3))
+    rng.shuffle(tasks)
+    S = 4
+    cu = torch.tensor(starts + [L], dtype=torch.int32, device="cuda")
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block, cu_seqlens=cu)  # the full softmax of every row
+    dk = torch.full((S, L, Hk, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    dv = torch.full((S, L, Hk, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    dq, dk, dv = bd.bdlm_attn_bwd_tasks(x.q, x.k, x.v, o, lse, x.do, block, tasks, S, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, cu_seqlens=np.array(starts + [L]), do=do64)
+    ref = [dict(seq_start=t.seq_start, n=t.n, q_lo=t.q_lo, q_hi=t.q_hi, key_lo=t.key_lo, key_hi=t.key_hi,
+                slot=t.slot) for t in tasks]
+    rq, rk, rv = oracle.task_attention_bwd(q64, k64, v64, full["o"], full["lse"], do64, block, w.scale, ref, S)
+    check_grad(host(dq), rq, "dq (sum over the tasks)")
+    gk, gv = host(dk), host(dv)
+    for s in range(S):
+        cov = ~np.isnan(rk[s, :, 0, 0])
+        check_grad(gk[s][cov], rk[s][cov], f"slot {s} dk")
+        check_grad(gv[s][cov], rv[s][cov], f"slot {s} dv")
+        assert np.all(gk[s][~cov] == 7.0) and np.all(gv[s][~cov] == 7.0), f"slot {s}: uncovered keys written"
+    # slots 0-2 partition every sequence's rows x keys: their sum is the full gradient
+    check_grad(gk[:3].sum(axis=0), full["dk"], "dk summed over the row-range slots")
+    check_grad(gv[:3].sum(axis=0), full["dv"], "dv summed over the row-range slots")
