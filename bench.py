@@ -42,8 +42,8 @@ UNIT = "TFLOP/s"
 # while the sources it is compiled from are unchanged (checked by hash;
 # otherwise reported as null)
 TRAFFIC = {"kernel_sources": ['block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu', 'block_diffusion_lm_bdlm_gb300/csrc/common.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/tc_ptx.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/kernels.h'],
-           "sha1": "e1352b8ba7ec9e14bea9c857e8a767840a958389",
-           "bytes_per_launch": 399730392320 + 211021425664,
+           "sha1": "cc4cad862cc766bfdd5dd5084d196dcaf57b2897",
+           "bytes_per_launch": 435731397120 + 233797456640,
            "note": "bwd_tc_kernel on this workload, ncu dram__bytes_read.sum + dram__bytes_write.sum"}
 
 

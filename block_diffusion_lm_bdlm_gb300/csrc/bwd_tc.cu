@@ -128,10 +128,23 @@ __device__ __forceinline__ bool named_and(int id, int n, bool v) {
     return r != 0;
 }
 
+// Item -> (key tile, kv head). Tiles are ordered heaviest first. By default
+// (K = 1) the items of one tile (its kv heads) are consecutive, so the order
+// is strictly heaviest first. For packed documents with many tiles the items
+// go in blocks of K = gridDim.x / 2 tiles, kv head by kv head within a block
+// (one wave of gridDim.x items spans two kv heads): measured on a GB300, this
+// takes the 64-document packed backward from 93.3 to 85.1 ms, while single
+// long sequences ran about 1 % faster with K = 1 (their DRAM traffic drops
+// about 4x with the blocks, but they are not bound by it).
 __device__ __forceinline__ ItemCtx decode(const BwdArgs& a, int item) {
     ItemCtx c;
-    c.kt = a.table[item / a.Hk];
-    c.kvh = item % a.Hk;
+    const int nt = a.hdr->n_tiles;
+    const bool packed = a.lay.mode == MODE_FULL && a.lay.cu != nullptr;
+    const int K = packed && nt >= 8 * (int)gridDim.x ? (int)gridDim.x / 2 : 1;
+    const int per = K * a.Hk;
+    const int ib = item / per, ir = item % per, kb = imin(K, nt - ib * K);
+    c.kt = a.table[ib * K + ir % kb];
+    c.kvh = ir / kb;
     c.k0 = key_row0(a.lay, c.kt);
     c.kv_rows = c.kt.nrows;
     const KeyRows r = key_tile_rows(a.lay, c.kt);

@@ -138,6 +138,39 @@ def test_long128k_sharded_forward_merge_backward(bd):
     assert rel <= 1e-2, f"sum of dq shares: {rel:.3e}"
 
 
+def test_long128k_task_lists(bd):
+    # the CSBP windows of the 128K workload as one forward task list and one
+    # backward task list, against the window calls and the full backward
+    w = synth.BY_NAME["long128k_n131072_b64_h32kv8_d128"]
+    x = synth.make_inputs(w, device="cuda")
+    n, B = w.n, w.block
+    windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+    wsf, wsb = workspaces(bd, w, 2 * n)
+    tasks = [bd.Task(0, n, 0, 2 * n, lo, hi, i) for i, (lo, hi) in enumerate(windows)]
+    so, sl = bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, B, tasks, len(tasks))
+    torch.cuda.synchronize()
+    for i, (lo, hi) in enumerate(windows):  # same tiles, same arithmetic: the same bits
+        po, pl = bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], B, part=bd.Partial.window(lo, hi), workspace=wsf)
+        assert bd.bdlm_read_error(wsf) == 0
+        assert torch.equal(so[i], po) and torch.equal(sl[i], pl), f"window {i}"
+        del po, pl
+    o, lse = bd.bdlm_lse_merge([so[i] for i in range(len(tasks))], [sl[i] for i in range(len(tasks))])
+    del so, sl
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, workspace=wsb)
+    assert bd.bdlm_read_error(wsb) == 0
+    bwd_tasks = [bd.Task(0, n, 0, 2 * n, lo, hi, 0) for lo, hi in windows]
+    tq, tk, tv = bd.bdlm_attn_bwd_tasks(x.q, x.k, x.v, o, lse, x.do, B, bwd_tasks, 1)
+    torch.cuda.synchronize()
+    for got, ref, nm in ((tq, dq, "dq"), (tk[0], dk, "dk"), (tv[0], dv, "dv")):
+        rel = ((got.float() - ref.float()).norm() / ref.float().norm()).item()
+        assert rel <= 1e-2, f"{nm} of the backward task list: {rel:.3e}"
+    # and against the oracle on sampled blocks
+    nb = n // B
+    blocks = [(0, (nb - 1) * B), (0, n + (nb // 2) * B)]
+    sampled_rows_check(x, w, o, lse, tq, kv_groups=[5], blocks=blocks)
+    sampled_keys_check(x, w, tk[0], tv[0], g=5, n=n, key_blocks=[("clean", nb - 3), ("corrupted", nb - 1)])
+
+
 def test_vlong256k_block_groups_and_backward(bd):
     w = synth.BY_NAME["vlong256k_n262144_b16_h16kv4_d128"]
     x = synth.make_inputs(w, device="cuda")
