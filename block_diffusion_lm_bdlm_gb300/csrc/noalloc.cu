@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB: enough for ~2.6 M rows
+constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB: enough for ~2.5 M rows
 
 static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 

@@ -162,7 +162,7 @@ BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * fixed 4 MiB array inside the library, which every GPU that loads the
  * library holds until the process exits. That bounds the call size: when
  * bdlm_attn_fwd_workspace_bytes(L, heads, head_dim, n_docs) exceeds 4 MiB
- * (about 2.6 million rows for one sequence) the call returns
+ * (about 2.5 million rows for one sequence) the call returns
  * BDLM_ERR_WORKSPACE and launches nothing; use bdlm_attn_fwd then.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -621,3 +621,48 @@ def test_task_list_backward(bd, ns, block, H, Hk, d):
     # slots 0-2 partition every sequence's rows x keys: their sum is the full gradient
     check_grad(gk[:3].sum(axis=0), full["dk"], "dk summed over the row-range slots")
     check_grad(gv[:3].sum(axis=0), full["dv"], "dv summed over the row-range slots")
+
+
+def test_task_list_with_many_tasks(bd):
+    # 1200 one-row tasks: more than one upload launch (960 records each) and
+    # more than one enumeration chunk (1024 tasks each), forward and backward
+    ns = (120, 80)
+    block, H, Hk, d = 16, 2, 1, 128
+    L = 2 * sum(ns)
+    starts = [0, 2 * ns[0]]
+    w, x = gen(ns[0], block, H, Hk, d, seed=97, L=L)
+    fwd_tasks, bwd_tasks = [], []
+    slot = 0
+    for s0, n in zip(starts, ns):
+        kc = [0, n // 2, n + 5, 2 * n]
+        for p in range(2 * n):
+            for wi, (ka, kb) in enumerate(zip(kc[:-1], kc[1:])):
+                fwd_tasks.append(bd.Task(s0, n, p, p + 1, ka, kb, wi))
+                bwd_tasks.append(bd.Task(s0, n, p, p + 1, ka, kb, slot))
+            slot += 1
+    assert len(fwd_tasks) == 1200
+    o, lse = bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, block, fwd_tasks, 3)
+    assert bd.bdlm_last_launch_count() == 4  # two uploads, prologue, attention
+    cu = torch.tensor(starts + [L], dtype=torch.int32, device="cuda")
+    fo, fl = bd.bdlm_attn_fwd(x.q, x.k, x.v, block, cu_seqlens=cu)
+    dq, dk, dv = bd.bdlm_attn_bwd_tasks(x.q, x.k, x.v, fo, fl, x.do, block, bwd_tasks, slot)
+    torch.cuda.synchronize()
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    ref = lambda ts: [dict(seq_start=t.seq_start, n=t.n, q_lo=t.q_lo, q_hi=t.q_hi, key_lo=t.key_lo,
+                           key_hi=t.key_hi, slot=t.slot) for t in ts]
+    ro, rl = oracle.task_attention(q64, k64, v64, block, w.scale, ref(fwd_tasks), 3)
+    for s in range(3):
+        check_o(host(o[s]), ro[s], f"slot {s} o")
+        check_lse(host(lse[s]), rl[s], f"slot {s} lse")
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, cu_seqlens=np.array(starts + [L]), do=do64)
+    rq, rk, rv = oracle.task_attention_bwd(q64, k64, v64, full["o"], full["lse"], do64, block, w.scale,
+                                           ref(bwd_tasks), slot)
+    check_grad(host(dq), rq, "dq")
+    # each slot holds one row's contribution to its sequence's keys: compare the
+    # sums over the slots (the full gradients) and every slot's covered keys
+    gk, gv = host(dk), host(dv)
+    check_grad(gk.sum(axis=0), full["dk"], "dk over all slots")
+    check_grad(gv.sum(axis=0), full["dv"], "dv over all slots")
+    cov = ~np.isnan(rk[:, :, 0, 0])
+    err = np.abs(gk[cov] - rk[cov]).max()
+    assert err <= 2e-2, f"per-slot dk max abs err {err:.3e}"
