@@ -515,7 +515,7 @@ def end_to_end(step, x, flops, args, world, dev):
                     h.copy_(t, non_blocking=True)
         comp.wait_stream(cs)
         t1.record(comp)
-        return t0, ev_done, t1
+        return t0, ev_in, ev_done, t1
 
     pipeline(2)  # untimed: the first use of freshly pinned host buffers is slow
     torch.cuda.synchronize()
@@ -523,7 +523,7 @@ def end_to_end(step, x, flops, args, world, dev):
     sampler = ClockSampler(dev.index, tag="e2e")
     sampler.start()
     barrier(world, dev)
-    t0, ev_done, t1 = pipeline(e2e_steps)
+    t0, ev_in, ev_done, t1 = pipeline(e2e_steps)
     torch.cuda.synchronize()
     barrier(world, dev)
     clocks = sampler.stop()
@@ -534,6 +534,8 @@ def end_to_end(step, x, flops, args, world, dev):
     return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": e2e_steps, "total_ms": e2e_ms,
             "compute_done_ms": [marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps)],
+            # the exposed head: step 0's inputs arriving, then step 0's compute
+            "first_copy_in_ms": t0.elapsed_time(ev_in[0]), "first_step_ms": ev_in[0].elapsed_time(ev_done[0]),
             "overlap": "copy stream; inputs of step k+1 in and results of step k out during compute",
             "clocks": clocks}
 
