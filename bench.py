@@ -275,7 +275,9 @@ class Step:
         self.ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs), dtype=torch.uint8, device=dev)
         self.launches = 0
 
-    def run(self, ev=None):
+    def run(self, ev=None, after_fwd=None):
+        """One step; `after_fwd` (if given) is called between the forward
+        (with its merge) and the backward."""
         bd, w, x = self.bd, self.w, self.x
         launches = 0
         if ev:
@@ -294,6 +296,8 @@ class Step:
             launches += bd.bdlm_last_launch_count()
         if ev:
             ev[2].record()
+        if after_fwd:
+            after_fwd()
         bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, cu_seqlens=self.cu, dq=self.dq, dk=self.dk,
                          dv=self.dv, workspace=self.ws_b)
         launches += bd.bdlm_last_launch_count()
@@ -468,8 +472,10 @@ def end_to_end(step, x, flops, args, world, dev):
     brings step k+1's inputs in from pinned host memory while step k computes
     and takes step k's results out to pinned host memory while step k+1
     computes. Every step's inputs are copied in and every step's results
-    copied out inside the timed region; only the first copy-in and the last
-    copy-out are not hidden behind compute."""
+    copied out inside the timed region. Only the head and the tail are not
+    hidden behind compute: step 0's q, k, v (its dO arrives during its
+    forward) and the last step's dq, dk, dv (its o and lse leave during its
+    backward)."""
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
     h_in = [pin(t) for t in (x.q, x.k, x.v, x.do)]
     for h, t in zip(h_in, (x.q, x.k, x.v, x.do)):
@@ -488,18 +494,32 @@ def end_to_end(step, x, flops, args, world, dev):
 
     def pipeline(K):
         t0, t1 = Ev(), Ev()
-        ev_in = [Ev() for _ in range(K)]    # inputs of step k are on the device
+        ev_in = [Ev() for _ in range(K)]    # q, k, v of step k are on the device
+        ev_do = [Ev() for _ in range(K)]    # dO of step k is on the device
+        ev_fwd = [Ev() for _ in range(K)]   # step k's o, lse are final (forward and merge done)
         ev_done = [Ev() for _ in range(K)]  # step k computed
+
+        def copy_in(k):  # on the copy stream: q, k, v first (the forward needs them), then dO
+            dst = ins(steps[k % 2])
+            for h, t in zip(h_in[:3], dst[:3]):
+                t.copy_(h, non_blocking=True)
+            ev_in[k].record(cs)
+            dst[3].copy_(h_in[3], non_blocking=True)
+            ev_do[k].record(cs)
+
         t0.record(comp)
         cs.wait_event(t0)
         with torch.cuda.stream(cs):
-            for h, t in zip(h_in, ins(steps[0])):
-                t.copy_(h, non_blocking=True)
-            ev_in[0].record(cs)
+            copy_in(0)
         for k in range(K):
             st = steps[k % 2]
             comp.wait_event(ev_in[k])
-            st.run()
+
+            def between(k=k):  # o, lse can go out now; the backward needs dO
+                ev_fwd[k].record(comp)
+                comp.wait_event(ev_do[k])
+
+            st.run(after_fwd=between)
             ev_done[k].record(comp)
             with torch.cuda.stream(cs):
                 if k + 1 < K:
@@ -507,11 +527,13 @@ def end_to_end(step, x, flops, args, world, dev):
                     # results went out before this copy (same stream)
                     if k >= 1:
                         cs.wait_event(ev_done[k - 1])
-                    for h, t in zip(h_in, ins(steps[(k + 1) % 2])):
-                        t.copy_(h, non_blocking=True)
-                    ev_in[k + 1].record(cs)
+                    copy_in(k + 1)
+                res = outs(st)
+                cs.wait_event(ev_fwd[k])
+                for h, t in zip(h_out[:2], res[:2]):  # o, lse during the backward
+                    h.copy_(t, non_blocking=True)
                 cs.wait_event(ev_done[k])
-                for h, t in zip(h_out, outs(st)):
+                for h, t in zip(h_out[2:], res[2:]):  # dq, dk, dv
                     h.copy_(t, non_blocking=True)
         comp.wait_stream(cs)
         t1.record(comp)
@@ -536,7 +558,8 @@ def end_to_end(step, x, flops, args, world, dev):
             "compute_done_ms": [marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps)],
             # the exposed head: step 0's inputs arriving, then step 0's compute
             "first_copy_in_ms": t0.elapsed_time(ev_in[0]), "first_step_ms": ev_in[0].elapsed_time(ev_done[0]),
-            "overlap": "copy stream; inputs of step k+1 in and results of step k out during compute",
+            "overlap": "copy stream; inputs of step k+1 in and results of step k out during compute; "
+                       "dO arrives during the forward, o and lse leave during the backward",
             "clocks": clocks}
 
 
