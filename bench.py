@@ -343,6 +343,66 @@ class Step:
         del ws_b
         return out[0], out[1]
 
+    def time_groups(self, reps=2):
+        """Block parallelism on one GPU: the forward and the backward of each
+        early/late block group of the workload (the corrupted rows of its
+        blocks against all clean keys and their own corrupted keys), the
+        groups run one after another; not part of the timed step. Inputs are
+        gathered before timing. Returns (fwd ms, bwd ms, fwd FLOP, bwd FLOP)
+        medians over `reps` runs after one warm-up, or None without groups."""
+        bd, w, x = self.bd, self.w, self.x
+        if not w.groups or w.docs:
+            return None
+        n, B = w.n, w.block
+        dev = x.q.device
+        groups = synth.early_late_groups(n // B, w.groups)
+        ar = torch.arange(B, device=dev)
+        clean = torch.arange(n, device=dev)
+        L, H, d = x.q.shape
+        ws_f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d), dtype=torch.uint8, device=dev)
+        gs = []
+        pairs = 0
+        for blocks in groups:
+            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
+            corr = (n + bl.long()[:, None] * B + ar[None]).reshape(-1)
+            kpos = torch.cat([clean, corr])
+            g = dict(bl=bl, q=x.q[corr].contiguous(), k=x.k[kpos].contiguous(), v=x.v[kpos].contiguous(),
+                     do=x.do[corr].contiguous())
+            g["o"] = torch.empty_like(g["q"])
+            g["lse"] = torch.empty((H, g["q"].shape[0]), dtype=torch.float32, device=dev)
+            g["dq"], g["dk"], g["dv"] = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+            gs.append(g)
+            # a corrupted row of block b sees b*B clean keys and its B own keys
+            pairs += sum(B * (b * B + B) for b in blocks)
+        f_fwd, f_bwd = 4 * d * H * pairs, 10 * d * H * pairs
+
+        def fwd():
+            for g in gs:
+                bd.bdlm_attn_fwd(g["q"], g["k"], g["v"], B, L=2 * n, part=bd.Partial.group(g["bl"]), out=g["o"],
+                                 lse=g["lse"], workspace=ws_f)
+
+        def bwd():
+            for g in gs:
+                bd.bdlm_attn_bwd(g["q"], g["k"], g["v"], g["o"], g["lse"], g["do"], B, L=2 * n,
+                                 part=bd.Partial.group(g["bl"]), dq=g["dq"], dk=g["dk"], dv=g["dv"], workspace=ws_b)
+
+        out = []
+        for f in (fwd, bwd):
+            f()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                f()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            out.append(statistics.median(times))
+        del gs, ws_f, ws_b
+        torch.cuda.empty_cache()
+        return out[0], out[1], f_fwd, f_bwd
+
     def time_running_merge(self, reps=2):
         """The same windows merged by the forward's epilogue into a running
         fp32 (o, lse) instead of kept as partials and merged (not part of the
@@ -458,12 +518,13 @@ def run_cuda(args, rank, world, local):
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     run_ms = step.time_running_merge()
     task_ms, task_bwd_ms = step.time_task_list()
+    groups = step.time_groups()
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms,
-            task_bwd_ms)
+            task_bwd_ms, groups)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -571,7 +632,8 @@ def l2_note(x):
 
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
-            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms, task_bwd_ms):
+            bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms, task_bwd_ms,
+            groups=None):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -603,6 +665,11 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "fwd_task_list_tflops": f_fwd / (task_ms / 1e3) / 1e12 if task_ms else None,
             "bwd_task_list_ms": task_bwd_ms,
             "bwd_task_list_tflops": f_bwd / (task_bwd_ms / 1e3) / 1e12 if task_bwd_ms else None,
+            # block groups (block parallelism): every group's forward, then every group's backward
+            "groups_fwd_ms": groups[0] if groups else None,
+            "groups_fwd_tflops": groups[2] / (groups[0] / 1e3) / 1e12 if groups else None,
+            "groups_bwd_ms": groups[1] if groups else None,
+            "groups_bwd_tflops": groups[3] / (groups[1] / 1e3) / 1e12 if groups else None,
             "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
             # the forward's secondary bound: one exponential per valid (row, key) pair and head
             "fwd_exp_per_s": f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3),
