@@ -208,6 +208,35 @@ def _bf16_cuda(name, t):
         raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
 
 
+def _shape(name, t, shape):
+    """The library reads and writes exactly the rows the call describes, so a
+    tensor of another shape would be read or written out of bounds."""
+    if tuple(t.shape) != tuple(int(v) for v in shape):
+        raise ValueError(f"{name} must be shaped {tuple(int(v) for v in shape)}, got {tuple(t.shape)}")
+
+
+def _call_rows(L: int, part: Optional[Partial], block: int):
+    """(rows of q, rows of k) that a call with total rows L and restriction
+    `part` reads, as include/bdlm.h defines them."""
+    if part is None or part.kind == PART_NONE:
+        return L, L
+    if part.kind == PART_KEY_WINDOW:
+        return (part.q_hi - part.q_lo if part.row_range else L), part.key_hi - part.key_lo
+    if part.q_blocks is None:
+        raise ValueError("a block group needs its q_blocks")
+    nq = part.q_blocks.numel() * block
+    return nq, L // 2 + nq
+
+
+def _check_qkv(q, k, v, L, part, block):
+    Lq, Lk = _call_rows(L, part, block)
+    d = q.shape[2]
+    _shape("q", q, (Lq, q.shape[1], d))
+    _shape("k", k, (Lk, k.shape[1], d))
+    _shape("v", v, k.shape)
+    return Lq, Lk
+
+
 def _cu(cu_seqlens):
     if cu_seqlens is None:
         return None, 1
@@ -269,6 +298,7 @@ def bdlm_attn_fwd(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=No
     Lq, H, d = q.shape
     Hk = k.shape[1]
     L = _total_rows(q, L, part)
+    _check_qkv(q, k, v, L, part, block)
     cu_ptr, n_docs = _cu(cu_seqlens)
     out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
     ws_bytes = lib.bdlm_attn_fwd_workspace_bytes(L, H, d, n_docs)
@@ -299,6 +329,8 @@ def bdlm_attn_fwd_tasks(q, k, v, block: int, tasks: Sequence[Task], n_slots: int
         _bf16_cuda(nm, t)
     L, H, d = q.shape
     Hk = k.shape[1]
+    _shape("k", k, (L, Hk, d))
+    _shape("v", v, k.shape)
     if out is None:
         out = torch.zeros((n_slots, L, H, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -338,6 +370,10 @@ def bdlm_attn_bwd_tasks(q, k, v, o, lse, dO, block: int, tasks: Sequence[Task], 
         _bf16_cuda(nm, t)
     L, H, d = q.shape
     Hk = k.shape[1]
+    _shape("k", k, (L, Hk, d))
+    _shape("v", v, k.shape)
+    _shape("o", o, q.shape)
+    _shape("dO", dO, q.shape)
     if dq is None:
         dq = torch.empty_like(q)
     if dk is None:
@@ -345,6 +381,7 @@ def bdlm_attn_bwd_tasks(q, k, v, o, lse, dO, block: int, tasks: Sequence[Task], 
     if dv is None:
         dv = torch.zeros((n_slots, L, Hk, d), dtype=torch.bfloat16, device=q.device)
     _bf16_cuda("dq", dq)
+    _shape("dq", dq, q.shape)
     for nm, t in (("dk", dk), ("dv", dv)):
         _bf16_cuda(nm, t)
         if tuple(t.shape) != (n_slots, L, Hk, d):
@@ -375,6 +412,7 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
     Lq, H, d = q.shape
     Hk = k.shape[1]
     L = _total_rows(q, L, part)
+    _check_qkv(q, k, v, L, part, block)
     cu_ptr, n_docs = _cu(cu_seqlens)
     out, lse, o_dtype = _fwd_outputs(q, part, out, lse)
     cpart = ctypes.byref(part.c(o_dtype)) if part is not None else None
@@ -397,10 +435,18 @@ def bdlm_attn_bwd(q, k, v, o, lse, dO, block: int, *, L: Optional[int] = None, c
     Lq, H, d = q.shape
     Hk = k.shape[1]
     L = _total_rows(q, L, part)
+    _check_qkv(q, k, v, L, part, block)
     cu_ptr, n_docs = _cu(cu_seqlens)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for nm, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _bf16_cuda(nm, t)
+    for nm, t, ref in (("o", o, q), ("dO", dO, q), ("dq", dq, q), ("dk", dk, k), ("dv", dv, k)):
+        _shape(nm, t, ref.shape)
+    _shape("lse", lse, (H, Lq))
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor")
     ws_bytes = lib.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
@@ -432,6 +478,11 @@ def bdlm_lse_merge(partials: Sequence[torch.Tensor], lses: Sequence[torch.Tensor
         out = torch.empty((rows, H, d), dtype=torch.bfloat16, device=partials[0].device)
     if lse is None:
         lse = torch.empty((H, rows), dtype=torch.float32, device=partials[0].device)
+    _bf16_cuda("out", out)
+    _shape("out", out, (rows, H, d))
+    _shape("lse", lse, (H, rows))
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor")
     pp = (ctypes.c_void_p * P)(*[p.data_ptr() for p in partials])
     lp = (ctypes.c_void_p * P)(*[l.data_ptr() for l in lses])
     st = lib.bdlm_lse_merge(pp, lp, P, BDLM_F32 if dt == torch.float32 else BDLM_BF16, rows, H, d,

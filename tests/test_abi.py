@@ -246,3 +246,29 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(64, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         bd.bdlm_attn_fwd(q, q, q, 16)
+
+
+def test_binding_derives_the_rows_a_call_reads(lib):
+    # the rows of q and k the C ABI reads for each kind of call; the binding
+    # refuses tensors of other shapes before anything reaches the GPU
+    import torch
+
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    assert bd._call_rows(512, None, 16) == (512, 512)
+    assert bd._call_rows(512, bd.Partial.window(64, 192), 16) == (512, 128)
+    assert bd._call_rows(512, bd.Partial.window(64, 192, q_lo=10, q_hi=50), 16) == (40, 128)
+    g = bd.Partial.group(torch.tensor([1, 3, 4], dtype=torch.int32))
+    assert bd._call_rows(512, g, 16) == (48, 256 + 48)
+    with pytest.raises(ValueError):
+        bd._call_rows(512, bd.Partial(bd.PART_BLOCK_GROUP), 16)
+    q = torch.empty(512, 4, 64)
+    bd._shape("q", q, (512, 4, 64))
+    with pytest.raises(ValueError, match="q must be shaped"):
+        bd._shape("q", q, (511, 4, 64))
+    k = torch.empty(128, 2, 64)
+    assert bd._check_qkv(q, k, torch.empty(128, 2, 64), 512, bd.Partial.window(64, 192), 16) == (512, 128)
+    with pytest.raises(ValueError, match="k must be shaped"):
+        bd._check_qkv(q, torch.empty(120, 2, 64), torch.empty(120, 2, 64), 512, bd.Partial.window(64, 192), 16)
+    with pytest.raises(ValueError, match="v must be shaped"):
+        bd._check_qkv(q, k, torch.empty(128, 2, 32), 512, bd.Partial.window(64, 192), 16)
