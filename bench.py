@@ -403,6 +403,31 @@ class Step:
         torch.cuda.empty_cache()
         return out[0], out[1], f_fwd, f_bwd
 
+    def time_graph(self, reps=5):
+        """The step captured once in a CUDA graph and replayed (every library
+        call only launches kernels on the current stream, with all host-side
+        values in kernel parameters). Returns the median ms per replay after
+        one warm-up replay; not part of the timed step."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        g.replay()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        del g
+        return statistics.median(times)
+
     def time_running_merge(self, reps=2):
         """The same windows merged by the forward's epilogue into a running
         fp32 (o, lse) instead of kept as partials and merged (not part of the
@@ -519,12 +544,13 @@ def run_cuda(args, rank, world, local):
     run_ms = step.time_running_merge()
     task_ms, task_bwd_ms = step.time_task_list()
     groups = step.time_groups()
+    graph_ms = step.time_graph()
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms,
-            task_bwd_ms, groups)
+            task_bwd_ms, groups, graph_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -633,7 +659,7 @@ def l2_note(x):
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms, task_bwd_ms,
-            groups=None):
+            groups=None, graph_ms=None):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -671,6 +697,9 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "groups_bwd_ms": groups[1] if groups else None,
             "groups_bwd_tflops": groups[3] / (groups[1] / 1e3) / 1e12 if groups else None,
             "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
+            # the same step replayed from a CUDA graph (outside the timed steps)
+            "step_graph_ms": graph_ms,
+            "step_graph_tflops": flops / (graph_ms / 1e3) / 1e12 if graph_ms else None,
             # the forward's secondary bound: one exponential per valid (row, key) pair and head
             "fwd_exp_per_s": f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3),
             "fwd_exp_frac_mufu": (f_fwd / (4 * w.head_dim) / (fwd_ms / 1e3)) / mufu_exp_peak(clocks),

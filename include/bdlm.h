@@ -32,6 +32,12 @@
  *     to an error word inside the workspace, read with bdlm_read_error.
  *   - Not thread-safe per workspace: two calls that share a workspace must be
  *     ordered on one stream.
+ *   - The compute calls (forward, backward, merge, task lists) only launch
+ *     kernels on `stream`, with every host-side value (task records, partial
+ *     pointer lists, tensor maps) in kernel parameters, so they can be
+ *     captured into a CUDA graph and replayed on new contents of the same
+ *     buffers. (bdlm_attn_fwd_noalloc must have run once on the device
+ *     before a capture; bdlm_read_error synchronises and cannot be captured.)
  */
 #ifndef BDLM_H
 #define BDLM_H

@@ -666,3 +666,59 @@ def test_task_list_with_many_tasks(bd):
     cov = ~np.isnan(rk[:, :, 0, 0])
     err = np.abs(gk[cov] - rk[cov]).max()
     assert err <= 2e-2, f"per-slot dk max abs err {err:.3e}"
+
+
+def test_step_captured_in_a_cuda_graph(bd):
+    # the library's compute calls only launch kernels on the given stream
+    # (kernel parameters carry every host-side value), so a whole step can be
+    # captured once and replayed on new inputs copied into the same buffers
+    n, block, H, Hk, d = 512, 32, 4, 2, 128
+    w, x = gen(n, block, H, Hk, d, seed=99)
+    L = 2 * n
+    wins = [(0, n // 2), (n // 2, n), (n, 2 * n)]
+    parts = [torch.empty_like(x.q) for _ in wins]
+    plse = [torch.empty((H, L), dtype=torch.float32, device="cuda") for _ in wins]
+    o = torch.empty_like(x.q)
+    lse = torch.empty((H, L), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v)
+    wsf = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d), dtype=torch.uint8, device="cuda")
+    tasks = [bd.Task(0, n, 0, L, lo, hi, i) for i, (lo, hi) in enumerate(wins)]
+    ws_t = torch.empty(bd.bdlm_attn_fwd_tasks_workspace_bytes(tasks), dtype=torch.uint8, device="cuda")
+    so = torch.empty((len(wins), L, H, d), dtype=torch.bfloat16, device="cuda")
+    sl = torch.empty((len(wins), H, L), dtype=torch.float32, device="cuda")
+
+    def step():
+        for (lo, hi), po, pl in zip(wins, parts, plse):
+            bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], block, part=bd.Partial.window(lo, hi), out=po, lse=pl,
+                             workspace=wsf)
+        bd.bdlm_lse_merge(parts, plse, out=o, lse=lse)
+        bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block, dq=dq, dk=dk, dv=dv, workspace=wsb)
+        bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, block, tasks, len(wins), out=so, lse=sl, workspace=ws_t)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (101, 102):
+        _, y = gen(n, block, H, Hk, d, seed=seed)
+        for dst, src in ((x.q, y.q), (x.k, y.k), (x.v, y.v), (x.do, y.do)):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (o, lse, dq, dk, dv, so, sl)]
+        step()  # the same step, eagerly
+        torch.cuda.synchronize()
+        ref = (o, lse, dq, dk, dv, so, sl)
+        for nm, a, b in zip(("o", "lse", "dk", "dv", "slots o", "slots lse"), [got[i] for i in (0, 1, 3, 4, 5, 6)],
+                            [ref[i] for i in (0, 1, 3, 4, 5, 6)]):
+            assert torch.equal(a, b), f"replay {seed}: {nm} differs from the eager step"
+        rel = ((got[2].float() - dq.float()).norm() / dq.float().norm()).item()
+        assert rel <= 1e-3, f"replay {seed}: dq {rel:.2e}"  # fp32 reduce-adds in another order
+        r = ref_full(y, w)
+        check_o(host(o), r["o"], "o")
+        check_grad(host(dq), r["dq"], "dq")
