@@ -270,10 +270,15 @@ def lse_merge(os, lses):
 # rit.work post: one rank owns whole target blocks and their corrupted K/V).
 # ----------------------------------------------------------------------------
 def group_positions(n, block, blocks):
-    """Doc-local positions of a group's query rows and of its key rows."""
+    """Doc-local positions of a group's query rows and of its key rows. Every
+    listed block takes `block` rows. When block does not divide n, the last
+    block of the corrupted half is short and its rows past the half's end are
+    padding, marked by position -1: they see no key and no row sees them."""
     blocks = np.asarray(blocks, dtype=np.int64)
     within = np.arange(block, dtype=np.int64)
-    corr = (n + blocks[:, None] * block + within[None, :]).reshape(-1)
+    lens = np.minimum(block, n - blocks * block)  # rows of each listed block
+    corr = n + blocks[:, None] * block + within[None, :]
+    corr = np.where(within[None, :] < lens[:, None], corr, -1).reshape(-1)
     qpos = corr
     kpos = np.concatenate([np.arange(n, dtype=np.int64), corr])
     return qpos, kpos
@@ -281,7 +286,8 @@ def group_positions(n, block, blocks):
 
 def group_attention(q_g, k_g, v_g, n, block, blocks, scale, do=None):
     qpos, kpos = group_positions(n, block, blocks)
-    m = mask_rows(qpos, n, block, kpos)
+    m = mask_rows(np.maximum(qpos, 0), n, block, np.maximum(kpos, 0))
+    m &= (qpos >= 0)[:, None] & (kpos >= 0)[None, :]  # padding rows and keys take no part
     o, lse = attend(q_g, k_g, v_g, m, scale)
     out = {"o": o, "lse": lse}
     if do is not None:

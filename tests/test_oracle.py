@@ -445,6 +445,40 @@ def test_block_groups_equal_unsplit():
     np.testing.assert_allclose(dv + clean["dv"], full["dv"], atol=1e-12)
 
 
+def test_block_groups_with_a_short_last_block():
+    # n = 62, B = 8: the last block of each half holds 6 rows. A group that
+    # lists it carries 2 padding rows (and keys) in its place: they take no
+    # part, and the real rows equal the unsplit rows.
+    n, block, H, Hk, d = 62, 8, 2, 1, 8
+    q, k, v, do = case(n, block, H, Hk, d, seed=85)
+    scale = 0.3
+    nb = -(-n // block)
+    full = oracle.bdlm_attention(q, k, v, block, scale, do=do)
+    groups = synth.early_late_groups(nb, 3)
+    assert any(nb - 1 in g for g in groups)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for blocks in groups:
+        qpos, kpos = oracle.group_positions(n, block, blocks)
+        pad_q, pad_k = qpos < 0, kpos < 0
+        assert pad_q.sum() == (2 if nb - 1 in blocks else 0)
+        take = lambda t, pos: np.where((pos >= 0)[:, None, None], t[np.maximum(pos, 0)], 0.0)
+        g = oracle.group_attention(take(q, qpos), take(k, kpos), take(v, kpos), n, block, blocks, scale,
+                                   do=take(do, qpos))
+        real = ~pad_q
+        np.testing.assert_allclose(g["o"][real], full["o"][qpos[real]], atol=1e-12)
+        np.testing.assert_allclose(g["lse"][:, real], full["lse"][:, qpos[real]], atol=1e-12)
+        np.testing.assert_allclose(g["dq"][real], full["dq"][qpos[real]], atol=1e-12)
+        assert np.all(g["o"][pad_q] == 0) and np.all(np.isneginf(g["lse"][:, pad_q])) and np.all(g["dq"][pad_q] == 0)
+        assert np.all(g["dk"][pad_k] == 0) and np.all(g["dv"][pad_k] == 0)
+        np.add.at(dk, kpos[~pad_k], g["dk"][~pad_k])
+        np.add.at(dv, kpos[~pad_k], g["dv"][~pad_k])
+    clean = oracle.bdlm_attention(q, k, v, block, scale, do=do,
+                                  row_blocks=[(0, b * block) for b in range(nb)])
+    np.testing.assert_allclose(dk + clean["dk"], full["dk"], atol=1e-12)
+    np.testing.assert_allclose(dv + clean["dv"], full["dv"], atol=1e-12)
+
+
 # --------------------------------------------------------------------------
 # packed documents: attention is confined to each document
 # --------------------------------------------------------------------------
