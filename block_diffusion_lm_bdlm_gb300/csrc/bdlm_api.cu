@@ -195,9 +195,9 @@ int check_common(const void* q, const void* k, const void* v, long long L, int b
         cm->Lk = part->key_hi - part->key_lo;
     } else {
         if (part->q_lo != 0 || part->q_hi != 0) return BDLM_ERR_INVALID_ARG;  // row ranges are for windows
-        // a group's q rows are B per listed block, so its sequence has whole blocks
-        if (n % block != 0) return BDLM_ERR_INVALID_ARG;
-        if (!part->q_blocks || part->n_q_blocks <= 0 || part->n_q_blocks > n / block) return BDLM_ERR_INVALID_ARG;
+        // B rows per listed block (a short last block is padded to B)
+        const long long nbk = (n + block - 1) / block;
+        if (!part->q_blocks || part->n_q_blocks <= 0 || part->n_q_blocks > nbk) return BDLM_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(part->q_blocks) & 3u) return BDLM_ERR_INVALID_ARG;
         lay->mode = MODE_GROUP;
         lay->blocks = part->q_blocks;

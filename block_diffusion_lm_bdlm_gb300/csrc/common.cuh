@@ -98,6 +98,11 @@ __host__ __device__ __forceinline__ int ld_ro(const int* p) {
 #endif
 }
 
+// Rows of block b of a half of length n (the last block is short when B does
+// not divide n). A block group gives every listed block B rows; the rows of
+// a short block past the half's end are padding.
+__host__ __device__ __forceinline__ int block_len(int n, int B, int b) { return imin(B, n - b * B); }
+
 // Key intervals of tile row r (empty intervals are [0, 0)).
 __host__ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile& t, int r) {
     Span s{0, 0, 0, 0};
@@ -107,9 +112,11 @@ __host__ __device__ __forceinline__ Span row_span(const Layout& lay, const Tile&
         const int j = t.pos0 + r;
         const int li = j / B;
         const int b = ld_ro(lay.blocks + li);
+        const int len = block_len(lay.n, B, b);
+        if (j - li * B >= len) return s;  // padding row of a short last block
         if (b > 0) { s.p_lo = 0; s.p_hi = b * B; }
         s.d_lo = lay.n + li * B;
-        s.d_hi = s.d_lo + B;
+        s.d_hi = s.d_lo + len;
         return s;
     }
     const int n = t.n;
@@ -160,6 +167,10 @@ __host__ __device__ __forceinline__ TileRange tile_range(const Layout& lay, cons
         if (s.d_hi > s.d_lo) {
             g.r2_lo = imin(g.r2_lo, s.d_lo);
             g.r2_hi = imax(g.r2_hi, s.d_hi);
+        }
+        if (lay.mode == MODE_GROUP) {  // padding rows of a short block in the tile see nothing
+            const int li = (t.pos0 + r) / B;
+            if (li * B + block_len(lay.n, B, ld_ro(lay.blocks + li)) < t.pos0 + t.nrows) g.full_hi = 0;
         }
         // first row of the next block; blocks are cut from the start of each
         // half (a group's list rows from 0), which is not a multiple of B when
@@ -233,17 +244,26 @@ __host__ __device__ __forceinline__ int key_row0(const Layout& lay, const Tile& 
 struct KeyRows {
     int a_lo, a_hi, b_lo, b_hi;
 };
+// Rows of a block group's list that hold real rows: all n_blocks * B, less
+// the padding of the short last block when the (ascending) list ends with it.
+__host__ __device__ __forceinline__ int group_rows_real(const Layout& lay) {
+    const int B = lay.B, nbk = (lay.n + B - 1) / B;
+    const int last = ld_ro(lay.blocks + lay.n_blocks - 1);
+    return (lay.n_blocks - 1) * B + (last == nbk - 1 ? block_len(lay.n, B, last) : B);
+}
+
 __host__ __device__ __forceinline__ KeyRows key_tile_rows(const Layout& lay, const Tile& t) {
     KeyRows r{0, 0, 0, 0};
     const int n = t.n, B = lay.B;
     if (lay.mode == MODE_GROUP) {
-        const int R = lay.n_blocks * B;
+        const int R = group_rows_real(lay);
         if (t.pos0 < n) {
             const int lo = group_count_le(lay, t.pos0 / B) * B;
             if (lo < R) { r.a_lo = lo; r.a_hi = R; }
         } else {
             r.a_lo = ((t.pos0 - n) / B) * B;
-            r.a_hi = ((t.pos0 + t.nrows - 1 - n) / B + 1) * B;
+            r.a_hi = imin(((t.pos0 + t.nrows - 1 - n) / B + 1) * B, R);
+            if (r.a_hi <= r.a_lo) { r.a_lo = 0; r.a_hi = 0; }  // padding keys only
         }
         return r;
     }
@@ -278,10 +298,15 @@ __host__ __device__ __forceinline__ KeyRows key_rows(const Layout& lay, const Ti
     if (lay.mode == MODE_GROUP) {
         if (kc < n) {
             r.a_lo = group_count_le(lay, kc / B) * B;
-            r.a_hi = lay.n_blocks * B;
+            r.a_hi = group_rows_real(lay);
+            if (r.a_hi <= r.a_lo) { r.a_lo = 0; r.a_hi = 0; }
         } else {
-            r.a_lo = ((kc - n) / B) * B;
-            r.a_hi = r.a_lo + B;
+            const int li = (kc - n) / B;
+            const int len = block_len(n, B, ld_ro(lay.blocks + li));
+            if (kc - n - li * B < len) {  // a real key: the real rows of its block
+                r.a_lo = li * B;
+                r.a_hi = r.a_lo + len;
+            }
         }
         return r;
     }

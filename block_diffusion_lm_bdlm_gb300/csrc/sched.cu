@@ -109,7 +109,7 @@ enumerate_kernel(Layout lay, int tile_rows, int key_tile, int kind, Tile* table,
         }
     }
     if (lay.mode == MODE_GROUP) {
-        const int nb = lay.n / lay.B;
+        const int nb = (lay.n + lay.B - 1) / lay.B;  // a short last block counts
         for (int i = tid; i < lay.n_blocks; i += kThreads) {
             int b = __ldg(lay.blocks + i);
             if (b < 0 || b >= nb) { bad = 1; bad_info = i; }

@@ -21,7 +21,7 @@
  *   - d is 64 or 128; H % Hk == 0; 1 <= B <= 1024; every document's clean
  *     length n is positive. Blocks are cut from the start of each half, so
  *     when B does not divide n the last block of each half holds n mod B rows
- *     (a BLOCK_GROUP call needs whole blocks: B must divide n).
+ *     (a BLOCK_GROUP call still gives that block B rows: see bdlm_partial).
  *   - The caller owns every buffer, including the workspace. The library never
  *     allocates or frees device memory and never synchronises, except in
  *     bdlm_read_error. Every call is asynchronous on `stream` (NULL = the
@@ -95,7 +95,12 @@ enum bdlm_part_flags {
  *   holds the corrupted rows of the listed blocks, B rows each, in list order
  *   (Lq = n_q_blocks * B). k and v hold the n clean rows followed by the same
  *   blocks' corrupted rows in the same order (Lk = n + n_q_blocks * B).
- *   q_blocks is a DEVICE array of distinct block ids in [0, n / B).
+ *   q_blocks is a DEVICE array of distinct block ids in [0, ceil(n / B)).
+ *   When B does not divide n, the last block (id ceil(n / B) - 1) holds
+ *   n mod B rows; listed, it still takes B rows of q (and of k, v), and the
+ *   rows past the half's end are padding: they see no key, no row sees them,
+ *   their o is 0, lse -inf and their gradients 0. Fill them with finite
+ *   values (zeros), since masked products still read them.
  *
  * flags (forward only):
  *   BDLM_PART_ACCUMULATE - KEY_WINDOW only. o and lse already hold the merged

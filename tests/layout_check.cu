@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -21,6 +22,7 @@ using namespace bdlm;
 namespace {
 
 bool visible(int p, int j, int n, int B) {
+    if (p < 0 || j < 0) return false;  // padding of a block group's short last block
     const bool qc = p < n, kc = j < n;
     const int qb = (qc ? p : p - n) / B, kb = (kc ? j : j - n) / B;
     if (qc) return kc && kb <= qb;
@@ -283,24 +285,28 @@ int main(int argc, char** argv) {
         // a task list over packed sequences
         check_tasks(tile_rows);
         ++checked;
-        // a block group (whole blocks), ascending list
-        {
-            const int nb = rnd(1, 12), Bg = rnd(1, 24), ng = nb * Bg;
+        // a block group, ascending list (forward and backward) and shuffled
+        // (forward); a short last block (B not dividing n) is padded to B rows
+        for (int shuffled = 0; shuffled < 2; ++shuffled) {
+            const int nb = rnd(1, 12), Bg = rnd(1, 24);
+            const int ng = nb * Bg - (rnd(0, 1) ? rnd(0, Bg - 1) : 0);
             Call c;
             std::memset(&c.lay, 0, sizeof(c.lay));
             for (int b = 0; b < nb; ++b)
-                if (rnd(0, 2) == 0) c.blocks.push_back(b);
-            if (c.blocks.empty()) c.blocks.push_back(rnd(0, nb - 1));
+                if (rnd(0, 2) == 0 || b == nb - 1) c.blocks.push_back(b);
+            if (shuffled)
+                for (int i = (int)c.blocks.size() - 1; i > 0; --i) std::swap(c.blocks[i], c.blocks[rnd(0, i)]);
             c.lay.mode = MODE_GROUP; c.lay.B = Bg; c.lay.n = ng; c.lay.n_docs = 1; c.lay.L = 2 * ng;
             c.lay.blocks = c.blocks.data(); c.lay.n_blocks = (int)c.blocks.size();
             c.n = ng; c.B = Bg;
+            auto pos = [&](int b, int i) { return i < ng - b * Bg ? ng + b * Bg + i : -1; };
             for (int b : c.blocks)
-                for (int i = 0; i < Bg; ++i) c.qpos.push_back(ng + b * Bg + i);
+                for (int i = 0; i < Bg; ++i) c.qpos.push_back(pos(b, i));
             for (int p = 0; p < ng; ++p) c.kpos.push_back(p);
             for (int b : c.blocks)
-                for (int i = 0; i < Bg; ++i) c.kpos.push_back(ng + b * Bg + i);
+                for (int i = 0; i < Bg; ++i) c.kpos.push_back(pos(b, i));
             check_forward(c, tile_rows);
-            check_backward(c, rnd(0, 1) ? 128 : 64);
+            if (!shuffled) check_backward(c, rnd(0, 1) ? 128 : 64);
             ++checked;
         }
     }

@@ -83,8 +83,10 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, q=None) == INVALID
     assert _fwd(lib, k=17) == INVALID            # misaligned
     assert _fwd(lib, L=255) == INVALID           # odd total length
-    p = bd._CPartial(bd.PART_BLOCK_GROUP, 1, 0, 0, 16)
-    assert _fwd(lib, L=200, part=ctypes.byref(p)) == INVALID  # a group needs whole blocks (n = 100, B = 16)
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 8, 0, 0, 16)
+    assert _fwd(lib, L=200, part=ctypes.byref(p)) == INVALID  # n = 100, B = 16: 7 blocks, the last one short
+    p = bd._CPartial(bd.PART_BLOCK_GROUP, 7, 0, 0, 16)
+    assert _fwd(lib, L=200, part=ctypes.byref(p), ws=None) == WS  # all 7 blocks: accepted up to the workspace
     assert _fwd(lib, heads=3, kv_heads=2) == INVALID
     assert _fwd(lib, head_dim=96) == UNSUP
     assert _fwd(lib, ws=None) == WS

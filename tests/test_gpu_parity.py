@@ -722,3 +722,51 @@ def test_step_captured_in_a_cuda_graph(bd):
         r = ref_full(y, w)
         check_o(host(o), r["o"], "o")
         check_grad(host(dq), r["dq"], "dq")
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,groups", [(300, 32, 4, 2, 128, 3), (200, 48, 2, 1, 128, 2),
+                                                   (100, 16, 2, 2, 64, 3), (150, 200, 2, 1, 128, 1)])
+def test_block_groups_with_a_short_last_block(bd, n, block, H, Hk, d, groups):
+    # B does not divide n: a group listing the short last block gives it B rows
+    # of q, k, v, the rows past the half's end being zero padding; the forward
+    # takes the list in any order, the backward ascending
+    w, x = gen(n, block, H, Hk, d, seed=19 + n)
+    nb = -(-n // block)
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    ws = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(2 * n, H, d, 1), dtype=torch.uint8, device="cuda")
+    lists = synth.early_late_groups(nb, groups)
+    assert any(nb - 1 in b for b in lists)
+
+    def take(t, pos):  # rows at positions `pos`, zeros for padding (-1)
+        p = torch.from_numpy(pos).cuda()
+        out = t[p.clamp(min=0)].clone()
+        out[p < 0] = 0
+        return out.contiguous()
+
+    def take64(t, pos):
+        return np.where((pos >= 0)[:, None, None], t[np.maximum(pos, 0)], 0.0)
+
+    for blocks in lists:
+        for order in (blocks, blocks[::-1]):
+            qpos, kpos = oracle.group_positions(n, block, order)
+            part = bd.Partial.group(torch.tensor(order, dtype=torch.int32, device="cuda"))
+            qg, kg, vg, dog = take(x.q, qpos), take(x.k, kpos), take(x.v, kpos), take(x.do, qpos)
+            go, gl = bd.bdlm_attn_fwd(qg, kg, vg, block, L=2 * n, part=part)
+            torch.cuda.synchronize()
+            r = oracle.group_attention(take64(q64, qpos), take64(k64, kpos), take64(v64, kpos), n, block, order,
+                                       w.scale, do=take64(do64, qpos))
+            check_o(host(go), r["o"], f"group {order} o")
+            check_lse(host(gl), r["lse"], f"group {order} lse")
+            real = torch.from_numpy(qpos >= 0).cuda()
+            assert torch.all(go[~real] == 0) and torch.all(torch.isneginf(gl[:, ~real]))
+            assert (go[real].float() - o[torch.from_numpy(qpos[qpos >= 0]).cuda()].float()).abs().max() <= 2e-2
+            if order != sorted(order):
+                continue
+            dq, dk, dv = bd.bdlm_attn_bwd(qg, kg, vg, go, gl, dog, block, L=2 * n, part=part, workspace=ws)
+            assert bd.bdlm_read_error(ws) == 0
+            check_grad(host(dq), r["dq"], f"group {order} dq")
+            check_grad(host(dk), r["dk"], f"group {order} dk")
+            check_grad(host(dv), r["dv"], f"group {order} dv")
+            pad_k = torch.from_numpy(kpos < 0).cuda()
+            assert torch.all(dq[~real] == 0) and torch.all(dk[pad_k] == 0) and torch.all(dv[pad_k] == 0)
