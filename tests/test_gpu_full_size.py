@@ -257,3 +257,36 @@ def test_packed_documents_full_size(bd):
     blocks = [(big, 0), (big, nd - B), (big, nd), (big, 2 * nd - B)]
     sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 5], blocks=blocks, cu=cu)
     identities_check(x, w, dk, dv)
+
+
+def test_packed_documents_as_task_lists(bd):
+    # the 64 packed documents as token-level tasks (each document: its rows
+    # against its clean keys into slot 0 and against its corrupted keys into
+    # slot 1), forward and backward in one launch each, against the varlen calls
+    w = synth.BY_NAME["packed64_b32_h32kv8_d128"]
+    x = synth.make_inputs(w, device="cuda")
+    cu = x.cu_seqlens
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    B, L = w.block, cu[-1]
+    wsf, wsb = workspaces(bd, w, L, len(cu) - 1)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, cu_seqlens=cu_d, workspace=wsf)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, cu_seqlens=cu_d, workspace=wsb)
+    assert bd.bdlm_read_error(wsb) == 0
+    tasks = []
+    for i in range(len(cu) - 1):
+        s0, n = int(cu[i]), int(cu[i + 1] - cu[i]) // 2
+        tasks += [bd.Task(s0, n, 0, 2 * n, 0, n, 0), bd.Task(s0, n, 0, 2 * n, n, 2 * n, 1)]
+    so, sl = bd.bdlm_attn_fwd_tasks(x.q, x.k, x.v, B, tasks, 2)
+    mo, ml = bd.bdlm_lse_merge([so[0], so[1]], [sl[0], sl[1]])
+    torch.cuda.synchronize()
+    assert (mo.float() - o.float()).abs().max().item() <= 2e-2
+    assert ((ml - lse).abs() / lse.abs().clamp(min=1.0)).max().item() <= 1e-3
+    del so, sl
+    # backward: each document's two windows have disjoint keys, so one slot holds them all
+    bt = [bd.Task(t.seq_start, t.n, t.q_lo, t.q_hi, t.key_lo, t.key_hi, 0) for t in tasks]
+    tq, tk, tv = bd.bdlm_attn_bwd_tasks(x.q, x.k, x.v, o, lse, x.do, B, bt, 1)
+    torch.cuda.synchronize()
+    for got, ref, nm in ((tq, dq, "dq"), (tk[0], dk, "dk"), (tv[0], dv, "dv")):
+        rel = ((got.float() - ref.float()).norm() / ref.float().norm()).item()
+        assert rel <= 1e-2, f"{nm} of the packed task list: {rel:.3e}"
+    identities_check(x, w, tk[0], tv[0])
