@@ -170,7 +170,8 @@ __host__ __device__ __forceinline__ TileRange tile_range(const Layout& lay, cons
         }
         if (lay.mode == MODE_GROUP) {  // padding rows of a short block in the tile see nothing
             const int li = (t.pos0 + r) / B;
-            if (li * B + block_len(lay.n, B, ld_ro(lay.blocks + li)) < t.pos0 + t.nrows) g.full_hi = 0;
+            const int len = block_len(lay.n, B, ld_ro(lay.blocks + li));
+            if (len < B && li * B + len < t.pos0 + t.nrows) g.full_hi = 0;
         }
         // first row of the next block; blocks are cut from the start of each
         // half (a group's list rows from 0), which is not a multiple of B when

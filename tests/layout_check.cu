@@ -75,6 +75,20 @@ void check_forward(const Call& c, int tile_rows) {
     const int hi = c.lay.mode == MODE_WINDOW ? c.lay.q_hi : (c.lay.mode == MODE_GROUP ? Lq : 2 * c.n);
     for (const Tile& t : tiles(lo, hi, split, tile_rows, c.n)) {
         const TileRange g = tile_range(c.lay, t);
+        // the unmasked range is exactly the keys every row's prefix holds:
+        // narrower only costs speed, wider would be wrong
+        {
+            int lo = -1, hi = 1 << 30;
+            for (int r = 0; r < t.nrows; ++r) {
+                const Span s = row_span(c.lay, t, r);
+                if (s.p_hi <= s.p_lo) { lo = 0; hi = 0; break; }
+                lo = lo > s.p_lo ? lo : s.p_lo;
+                hi = hi < s.p_hi ? hi : s.p_hi;
+            }
+            const bool want_empty = hi <= lo, got_empty = g.full_hi <= g.full_lo;
+            if (want_empty != got_empty || (!want_empty && (g.full_lo != lo || g.full_hi != hi)))
+                fail("full range not the rows' common prefix", c.n, c.B, t.pos0, g.full_lo, g.full_hi);
+        }
         const int BN = 128;
         const int n1 = (g.r1_hi - g.r1_lo + BN - 1) / BN, n2 = (g.r2_hi - g.r2_lo + BN - 1) / BN;
         for (int r = 0; r < t.nrows; ++r) {
