@@ -1,11 +1,13 @@
 // sched.cu - tile enumeration and ordering for the BDLM kernels.
 //
 // One small kernel, launched before every attention kernel, that
-//   1. clears the workspace header (error word, work counters);
-//   2. validates cu_seqlens / the block list on the device;
+//   1. clears the workspace header (error word, work counter);
+//   2. validates cu_seqlens / the block list on the device (a task list is
+//      checked on the host and reaches the device through task_upload_kernel);
 //   3. enumerates the row tiles of the call (never straddling a document half)
 //      with a cost estimate in key tiles (forward) or query rows (backward);
-//   4. orders them by descending cost with a counting sort.
+//   4. orders them by descending cost with a counting sort (for a task list,
+//      earlier tasks first among tiles of equal cost).
 // The attention kernels then take work items from the front of this list with
 // an atomic counter. Taking the heaviest remaining tile first is the
 // work-conserving form of pairing early and late blocks for balance (rit.work
