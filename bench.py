@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -99,10 +100,13 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # raw samples go to BDLM_CLOCKS_DIR (default: the system temporary
+    # directory); the JSON line carries their summary
     def __init__(self, index, tag="timed"):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{tag}_gpu{index}.csv")
+        d = os.environ.get("BDLM_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_{tag}_gpu{index}.csv")
 
     def start(self):
         try:
