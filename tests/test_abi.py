@@ -274,3 +274,41 @@ def test_binding_derives_the_rows_a_call_reads(lib):
         bd._check_qkv(q, torch.empty(120, 2, 64), torch.empty(120, 2, 64), 512, bd.Partial.window(64, 192), 16)
     with pytest.raises(ValueError, match="v must be shaped"):
         bd._check_qkv(q, k, torch.empty(128, 2, 32), 512, bd.Partial.window(64, 192), 16)
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    # the binding's ctypes mirrors of bdlm_partial and bdlm_task have the C
+    # header's size and field offsets (compiled here with the host compiler)
+    import shutil
+    import subprocess
+
+    import block_diffusion_lm_bdlm_gb300 as bd
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"bdlm_partial": [f for f, _ in bd._CPartial._fields_], "bdlm_task": [f for f, _ in bd._CTask._fields_]}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "bdlm.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'printf("{st} size %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'printf("{st} {f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for st, cls in (("bdlm_partial", bd._CPartial), ("bdlm_task", bd._CTask)):
+        assert got[(st, "size")] == ctypes.sizeof(cls), st
+        for f in fields[st]:
+            assert got[(st, f)] == getattr(cls, f).offset, (st, f)
+    # every field of the C structs is mirrored (no field missing from ctypes)
+    hdr = open(os.path.join(ROOT, "include", "bdlm.h")).read()
+    for st in fields:
+        body = hdr[:hdr.index("} " + st + ";")]
+        body = body[body.rindex("typedef struct {"):]
+        declared = re.findall(r"\b(\w+)\s*(?:,\s*(\w+)\s*)?;", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+        names = [x for pair in declared for x in pair if x]
+        assert sorted(names) == sorted(fields[st]), (st, names)
