@@ -4,7 +4,9 @@
 // One persistent CTA per SM takes work items (128-row query tile, pair of
 // query heads that share one kv head) from the ordered tile list. Both heads
 // of a pair see the same keys under the same mask, so one K/V stream in
-// shared memory feeds two 128-row MMA tiles.
+// shared memory feeds two 128-row MMA tiles. In a task list every tile
+// carries its task, which gives its key window (through the row spans) and
+// the output slot its rows are written to.
 //
 // Warp roles (384 threads, launched at 168 registers each):
 //   warps 0-3  softmax group 0 (head h0), one TMEM lane = one query row each
