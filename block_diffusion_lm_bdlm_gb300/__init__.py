@@ -401,11 +401,14 @@ def bdlm_attn_bwd_tasks(q, k, v, o, lse, dO, block: int, tasks: Sequence[Task], 
 
 def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_seqlens=None,
                           softmax_scale: float = 0.0, part: Optional[Partial] = None, out=None, lse=None,
-                          stream=None):
+                          stream=None, check: bool = False):
     """The forward without a workspace (see bdlm_attn_fwd_noalloc in
     include/bdlm.h): the library uses its own fixed scratch, so the call
     allocates nothing on the device beyond the outputs (pass `out` and `lse`
-    to allocate nothing at all)."""
+    to allocate nothing at all). Problems found on the device (a malformed
+    cu_seqlens or block list) leave o and lse unwritten and are reported by
+    bdlm_read_error(None); check=True synchronises the stream after the call
+    and raises BDLMError for them (not allowed under stream capture)."""
     lib = load_library()
     for nm, t in (("q", q), ("k", k), ("v", v)):
         _bf16_cuda(nm, t)
@@ -419,6 +422,8 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
     st = lib.bdlm_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), L,
                                    block, H, Hk, d, cu_ptr, n_docs, softmax_scale, cpart, _stream(stream))
     _check(st, "bdlm_attn_fwd_noalloc")
+    if check:
+        _check(bdlm_read_error(None, stream), "bdlm_attn_fwd_noalloc (device)")
     return out, lse
 
 
@@ -499,7 +504,9 @@ def bdlm_selftest_timeout(workspace: torch.Tensor, wait_ns: int = 100_000_000, s
     _check(st, "bdlm_selftest_timeout")
 
 
-def bdlm_read_error(workspace: torch.Tensor, stream=None) -> int:
+def bdlm_read_error(workspace: Optional[torch.Tensor], stream=None) -> int:
     """Synchronise the stream and return the device error word of the last call
-    that used `workspace` (0 = none)."""
-    return int(load_library().bdlm_read_error(workspace.data_ptr(), _stream(stream)))
+    that used `workspace` (0 = none). workspace=None reads the fixed scratch of
+    bdlm_attn_fwd_noalloc on the current device."""
+    ptr = None if workspace is None else workspace.data_ptr()
+    return int(load_library().bdlm_read_error(ptr, _stream(stream)))

@@ -509,7 +509,12 @@ int bdlm_lse_merge(const void* const* partials, const float* const* lses, int32_
 }
 
 int bdlm_read_error(const void* workspace, bdlm_stream_t stream) {
-    if (!workspace) return BDLM_ERR_INVALID_ARG;
+    if (!workspace) {  // the no-allocation forward's scratch on the current device
+        void* p = nullptr;
+        const int st = noalloc_scratch(&p);
+        if (st != BDLM_OK) return st;
+        workspace = p;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int word[2] = {0, 0};
     if (cudaMemcpyAsync(word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)

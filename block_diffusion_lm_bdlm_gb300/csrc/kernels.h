@@ -83,4 +83,8 @@ cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t st, int* laun
 cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st, int* launches);
 
+// Device address of the no-allocation forward's fixed scratch on the current
+// device (a bdlm_status; looked up again after the context changes).
+int noalloc_scratch(void** out);
+
 }  // namespace bdlm

@@ -8,11 +8,13 @@
 // and lse; the forward's own scratch (the tile table, the work counter and
 // the device error word) lives here instead, in a fixed array that every GPU
 // which loads this library holds until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "bdlm.h"
+#include "kernels.h"
 
 namespace {
 
@@ -21,26 +23,59 @@ constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB: enough for ~2.5 M r
 static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_addr[128] = {nullptr};  // device address of g_fwd_scratch, per device
+struct Cached {
+    CUcontext ctx;  // the context the address belongs to
+    void* addr;     // device address of g_fwd_scratch in that context
+};
+Cached g_cache[128] = {};
+
+// cuCtxGetCurrent through the runtime's driver entry-point query, so that the
+// library keeps no link-time dependency on the driver library (it loads, and
+// its host-side checks run, on machines without a GPU driver).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return nullptr;
+        fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    CUcontext c = nullptr;
+    if (fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 // Device address of the scratch on the current device. The name
 // g_fwd_scratch in host code is only a host-side stand-in; the address a
-// kernel may use comes from cudaGetSymbolAddress, taken once per device with
-// that device current.
+// kernel may use comes from cudaGetSymbolAddress, taken with the device
+// current. It is cached per device together with the context it was taken
+// in, and looked up again when that context changes (after a device reset
+// the runtime loads the module into a new primary context, at a new address).
 int scratch_on_current_device(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return BDLM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    Cached& c = g_cache[dev];
+    CUcontext ctx = current_context();
+    if (!c.addr || !ctx || ctx != c.ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || !p) return BDLM_ERR_CUDA;
-        g_addr[dev] = p;
+        c.addr = p;
+        c.ctx = current_context();  // the lookup makes the runtime's context current if it was not
     }
-    *out = g_addr[dev];
+    *out = c.addr;
     return BDLM_OK;
 }
 
 }  // namespace
+
+namespace bdlm {
+int noalloc_scratch(void** out) { return scratch_on_current_device(out); }
+}  // namespace bdlm
 
 extern "C" BDLM_API int bdlm_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                               int64_t L, int32_t block, int32_t heads, int32_t kv_heads,

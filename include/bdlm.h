@@ -177,11 +177,16 @@ BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * BDLM_ERR_WORKSPACE and launches nothing; use bdlm_attn_fwd then.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. Every call on a device shares the one array and each call clears
- * the parts that must start at zero; calls whose execution overlaps on the
- * GPU (other streams, or other host threads) race on it, so order them.
- * Device-detected errors land in the shared array and are not readable
- * through bdlm_read_error.
+ * capture. The address is kept together with the CUDA context it belongs to
+ * and looked up again when the device's current context changes (e.g. after
+ * cudaDeviceReset); that later lookup is again not allowed under capture.
+ * Every call on a device shares the one array and each call clears the parts
+ * that must start at zero; calls whose execution overlaps on the GPU (other
+ * streams, or other host threads) race on it, so order them.
+ * Device-detected errors (a malformed cu_seqlens or block list, a wait that
+ * timed out) land in the shared array, where they leave o and lse unwritten;
+ * bdlm_read_error(NULL, stream) returns the error word of the last call on
+ * the current device.
  */
 BDLM_API int bdlm_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                   int64_t L, int32_t block, int32_t heads, int32_t kv_heads, int32_t head_dim,
@@ -337,7 +342,8 @@ BDLM_API int bdlm_lse_merge(const void* const* partials, const float* const* lse
 
 /* Synchronises `stream`, then returns the device error word of the last call
  * that used `workspace` (BDLM_OK, BDLM_ERR_TIMEOUT or BDLM_ERR_DEVICE_CHECK),
- * or BDLM_ERR_CUDA if the stream reports a CUDA error. */
+ * or BDLM_ERR_CUDA if the stream reports a CUDA error. workspace == NULL
+ * reads the fixed scratch of bdlm_attn_fwd_noalloc on the current device. */
 BDLM_API int bdlm_read_error(const void* workspace, bdlm_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */

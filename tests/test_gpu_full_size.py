@@ -1,8 +1,18 @@
 """GPU parity at the full workload sizes, in the launch configuration the
-benchmark times. The oracle checks sampled query blocks one by one (o, lse
-and dq are row-local), complete dk/dv for sampled key blocks (every query
-block that sees them is recomputed), and identities that hold at any size:
-sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per kv head."""
+benchmark times. The float64 oracle checks, on every kv group of each
+workload:
+  - sampled query blocks one by one (o, lse and dq are row-local), spread
+    from the first to the last block of both halves;
+  - complete dk, dv of late clean key blocks and of corrupted key blocks
+    (every query block that sees them is recomputed);
+  - for early clean key blocks, whose complete gradient needs every row's
+    full softmax (the whole forward of a kv group), the contribution of
+    sampled query blocks, through the row-restricted key-window backward:
+    the same kernel, asked for one query block against one key block;
+and identities that hold at any size: sum_j dK_j = 0 and
+sum_j dV_j = sum_i dO_i per kv head. The 256K block groups are checked
+against the oracle directly (each group's earliest and latest blocks), not
+only against the unsplit call."""
 import numpy as np
 import pytest
 import torch
@@ -31,11 +41,16 @@ def f32(t):
     return t.float().cpu().numpy()
 
 
-def sampled_rows_check(x, w, o, lse, dq, kv_groups, blocks, cu=None):
+def host_group(x, w, g):
+    """q, k, v, dO of kv group g as float32 host arrays holding the bf16 values."""
+    return tuple(f32(t) for t in group_slices(x, w, g))
+
+
+def sampled_rows_check(x, w, o, lse, dq, kv_groups, blocks, cu=None, hg=None):
     """o, lse, dq of the given query blocks (doc, first row) against the oracle."""
     G = w.heads // w.kv_heads
     for g in kv_groups:
-        q, k, v, do = (f32(t) for t in group_slices(x, w, g))
+        q, k, v, do = hg if hg is not None else host_group(x, w, g)
         r = oracle.bdlm_attention(q, k, v, w.block, w.scale, cu_seqlens=cu, do=do, row_blocks=blocks,
                                   want_kv_grads=False)
         starts = [0] if cu is None else cu
@@ -44,15 +59,16 @@ def sampled_rows_check(x, w, o, lse, dq, kv_groups, blocks, cu=None):
         check_o(host(o[rows][:, hs]), r["o"][rows], f"o (kv group {g})")
         check_lse(host(lse[hs][:, rows]), r["lse"][:, rows], f"lse (kv group {g})")
         check_grad(host(dq[rows][:, hs]), r["dq"][rows], f"dq (kv group {g})")
+    return r
 
 
-def sampled_keys_check(x, w, dk, dv, g, n, key_blocks):
+def sampled_keys_check(x, w, dk, dv, g, n, key_blocks, hg=None):
     """Complete dk, dv of the clean key block b_c (seen by clean blocks >= b_c
     and corrupted blocks > b_c) and of corrupted key blocks (seen by their own
     block), for kv group g."""
     B = w.block
     nb = n // B
-    q, k, v, do = (f32(t) for t in group_slices(x, w, g))
+    q, k, v, do = hg if hg is not None else host_group(x, w, g)
     for kind, b in key_blocks:
         if kind == "clean":
             seers = [(0, bb * B) for bb in range(b, nb)] + [(0, n + bb * B) for bb in range(b + 1, nb)]
@@ -81,6 +97,40 @@ def identities_check(x, w, dk, dv):
     do_sum = x.do.double().view(x.do.shape[0], w.kv_heads, G, -1).sum((0, 2))
     rel = (dv_sum - do_sum).norm() / do_sum.norm()
     assert rel <= 1e-2, f"sum of dV differs from sum of dO: {rel:.3e}"
+
+
+def spread_blocks(n, B, shard_rows=0):
+    """16 query blocks, 8 per half: the first two, the two around the first
+    clean-shard boundary (if any), two in the middle and the last two. The
+    pairs straddle a 128-row forward tile boundary or sit inside one tile."""
+    nb = n // B
+    sh = shard_rows // B if shard_rows else nb // 4
+    clean = sorted({0, 1, sh - 1, sh, nb // 2 - 1, nb // 2, nb - 2, nb - 1})
+    corr = sorted({0, 1, sh - 1, sh, nb // 2, nb // 2 + 1, nb - 2, nb - 1})
+    return [(0, b * B) for b in clean] + [(0, n + b * B) for b in corr]
+
+
+def early_key_check(bd, x, w, o, lse, g, n, key_block, seer_blocks, ref, hg=None, ws=None):
+    """Contribution of each listed query block to dk, dv of one early clean key
+    block, for kv group g: the GPU's key-window backward restricted to that
+    query block's rows (o, lse: the merged full forward), against the
+    oracle's partial backward of the same rows and keys, taken with the
+    oracle's own full-row o and lse (`ref`, an oracle result that covers
+    the listed blocks)."""
+    B = w.block
+    lo, hi = key_block * B, (key_block + 1) * B
+    q, k, v, do = hg if hg is not None else host_group(x, w, g)
+    for _, r0 in seer_blocks:
+        rows = slice(r0, r0 + B)
+        part = oracle.partial_attention(q[rows], k[lo:hi], v[lo:hi], n, B, lo, hi, w.scale, do=do[rows],
+                                        o_full=ref["o"][rows], lse_full=ref["lse"][:, rows], q_lo=r0, q_hi=r0 + B)
+        _, gk, gv = bd.bdlm_attn_bwd(x.q[rows], x.k[lo:hi], x.v[lo:hi], o[rows], lse[:, rows].contiguous(),
+                                     x.do[rows], B, L=2 * n, part=bd.Partial.window(lo, hi, q_lo=r0, q_hi=r0 + B),
+                                     workspace=ws)
+        assert ws is None or bd.bdlm_read_error(ws) == 0
+        what = f"kv group {g}, key block {key_block} from rows {r0}"
+        check_grad(host(gk[:, g:g + 1]), part["dk"], "dk, " + what)
+        check_grad(host(gv[:, g:g + 1]), part["dv"], "dv, " + what)
 
 
 def test_long128k_sharded_forward_merge_backward(bd):
@@ -117,10 +167,20 @@ def test_long128k_sharded_forward_merge_backward(bd):
     assert ((rl - lse).abs() / lse.abs().clamp(min=1.0)).max().item() <= 1e-3
     del ro, rl
     nb = n // B
-    blocks = [(0, 0), (0, (nb // 2) * B), (0, (nb - 1) * B), (0, n), (0, n + (nb // 3) * B), (0, n + (nb - 1) * B)]
-    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 7], blocks=blocks)
-    sampled_keys_check(x, w, dk, dv, g=3, n=n, key_blocks=[("clean", nb - 1), ("clean", nb - 2), ("corrupted", 0),
-                                                           ("corrupted", nb // 2)])
+    # every kv group: 16 query blocks row by row; complete dk, dv of two late
+    # clean and two corrupted key blocks; two early clean key blocks through
+    # the contributions of query blocks from both halves
+    blocks = spread_blocks(n, B, shard_rows=n // w.shards)
+    for g in range(w.kv_heads):
+        hg = host_group(x, w, g)
+        ref = sampled_rows_check(x, w, o, lse, dq, kv_groups=[g], blocks=blocks, hg=hg)
+        sampled_keys_check(x, w, dk, dv, g=g, n=n, key_blocks=[("clean", nb - 1), ("clean", nb - 2),
+                                                               ("corrupted", 0), ("corrupted", nb // 2 + 1)], hg=hg)
+        early_key_check(bd, x, w, o, lse, g, n, 0, [(0, 0), (0, (nb // 2) * B), (0, (nb - 1) * B), (0, n + B),
+                                                    (0, n + (nb - 1) * B)], ref, hg=hg, ws=wsb)
+        early_key_check(bd, x, w, o, lse, g, n, nb // 2, [(0, (nb // 2) * B), (0, n + (nb // 2 + 1) * B)], ref,
+                        hg=hg, ws=wsb)
+        del hg, ref
     identities_check(x, w, dk, dv)
     # sharded backward: per-shard calls with the merged o and lse; the dq
     # shares sum to the unsharded dq and the shards' dk, dv tile it
@@ -180,9 +240,44 @@ def test_vlong256k_block_groups_and_backward(bd):
     o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, B, workspace=wsf)
     assert bd.bdlm_read_error(wsf) == 0
     groups = synth.early_late_groups(nb, w.groups)
+    G = w.heads // w.kv_heads
+    # the oracle's o, lse, dq of each group's earliest and latest block (the
+    # early/late pair that opens and closes its list), on kv group gi mod Hk
+    ref_rows = {}
+    for g in range(w.kv_heads):
+        mine = [gi for gi in range(len(groups)) if gi % w.kv_heads == g]
+        if not mine:
+            continue
+        q, k, v, do = host_group(x, w, g)
+        for gi in mine:
+            ends = (groups[gi][0], groups[gi][-1])
+            r = oracle.bdlm_attention(q, k, v, B, w.scale, do=do, row_blocks=[(0, n + b * B) for b in ends],
+                                      want_kv_grads=False)
+            for b in ends:
+                rows = slice(n + b * B, n + (b + 1) * B)
+                ref_rows[(gi, b)] = (r["o"][rows], r["lse"][:, rows], r["dq"][rows])
+        del q, k, v, do
+
+    def group_vs_oracle(gi, blocks, t, what):
+        """Rows of the group's earliest and latest block in a group call's
+        output t ([list rows, H, d], or [H, list rows] for lse) against the oracle."""
+        g = gi % w.kv_heads
+        hs = slice(g * G, (g + 1) * G)
+        for b in (blocks[0], blocks[-1]):
+            li = blocks.index(b)
+            lr = slice(li * B, (li + 1) * B)
+            ro, rl, rq = ref_rows[(gi, b)]
+            tag = f"group {gi} block {b} {what}"
+            if what == "o":
+                check_o(host(t[lr][:, hs]), ro, tag)
+            elif what == "lse":
+                check_lse(host(t[hs][:, lr]), rl, tag)
+            else:
+                check_grad(host(t[lr][:, hs]), rq, tag)
+
     worst_o, worst_l = 0.0, 0.0
     clean_pos = torch.arange(n, device="cuda")
-    for blocks in groups:
+    for gi, blocks in enumerate(groups):
         bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
         corr = (n + bl.long()[:, None] * B + torch.arange(B, device="cuda")[None]).reshape(-1)
         kpos = torch.cat([clean_pos, corr])
@@ -191,18 +286,25 @@ def test_vlong256k_block_groups_and_backward(bd):
         assert bd.bdlm_read_error(wsf) == 0
         worst_o = max(worst_o, (go.float() - o[corr].float()).abs().max().item())
         worst_l = max(worst_l, ((gl - lse[:, corr]).abs() / lse[:, corr].abs().clamp(min=1.0)).max().item())
+        group_vs_oracle(gi, blocks, go, "o")
+        group_vs_oracle(gi, blocks, gl, "lse")
     assert worst_o <= 2e-2 and worst_l <= 1e-3, (worst_o, worst_l)
     dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, B, workspace=wsb)
     assert bd.bdlm_read_error(wsb) == 0
-    # the early/late pair of group 0 and a middle block, clean and corrupted
-    blocks = [(0, 0), (0, (nb - 1) * B), (0, n), (0, n + (nb - 1) * B), (0, n + (nb // 2) * B)]
-    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 3], blocks=blocks)
-    sampled_keys_check(x, w, dk, dv, g=1, n=n, key_blocks=[("clean", nb - 1), ("corrupted", 5)])
+    # every kv group: 16 query blocks of the unsplit call row by row, complete
+    # dk, dv of late clean and of corrupted key blocks
+    blocks = spread_blocks(n, B)
+    for g in range(w.kv_heads):
+        hg = host_group(x, w, g)
+        sampled_rows_check(x, w, o, lse, dq, kv_groups=[g], blocks=blocks, hg=hg)
+        sampled_keys_check(x, w, dk, dv, g=g, n=n, key_blocks=[("clean", nb - 1), ("clean", nb - 2),
+                                                               ("corrupted", 5), ("corrupted", nb // 2)], hg=hg)
+        del hg
     identities_check(x, w, dk, dv)
     # block-group backward of every group: dq of the group's rows and dk, dv
-    # of its corrupted keys equal the unsplit backward's; for group 0, the
-    # group's share of dk, dv of a late clean key block against the oracle
-    G = w.heads // w.kv_heads
+    # of its corrupted keys equal the unsplit backward's, and its earliest and
+    # latest blocks' dq equal the oracle's; for group 0, the group's share of
+    # dk, dv of a late clean key block against the oracle
     for gi, blocks in enumerate(groups):
         bl = torch.tensor(blocks, dtype=torch.int32, device="cuda")
         corr = (n + bl.long()[:, None] * B + torch.arange(B, device="cuda")[None]).reshape(-1)
@@ -215,6 +317,7 @@ def test_vlong256k_block_groups_and_backward(bd):
         for got, ref, nm in ((gq, dq[corr], "dq"), (gk[n:], dk[corr], "dk"), (gv[n:], dv[corr], "dv")):
             rel = ((got.float() - ref.float()).norm() / ref.float().norm()).item()
             assert rel <= 1e-2, f"group {gi} {nm}: {rel:.3e}"
+        group_vs_oracle(gi, blocks, gq, "dq")
         if gi == 0:
             b = nb - 64  # seen by the group's blocks after it (a few late ones)
             seers = [(0, n + bb * B) for bb in blocks if bb > b]
@@ -251,11 +354,28 @@ def test_packed_documents_full_size(bd):
         check_grad(host(dq[s][:, 2 * G:3 * G]), r["dq"], "dq")
         check_grad(host(dk[s][:, 2:3]), r["dk"], "dk")
         check_grad(host(dv[s][:, 2:3]), r["dv"], "dv")
-    # sampled blocks of the longest document
-    big = max(range(len(lens)), key=lambda i: lens[i])
-    nd = lens[big] // 2
-    blocks = [(big, 0), (big, nd - B), (big, nd), (big, 2 * nd - B)]
-    sampled_rows_check(x, w, o, lse, dq, kv_groups=[0, 5], blocks=blocks, cu=cu)
+    # every kv group: the median-length document in full, and sampled blocks
+    # (first, middle and last of both halves) of the longest and the median one
+    order = sorted(range(len(lens)), key=lambda i: lens[i])
+    big, med = order[-1], order[len(order) // 2]
+    blocks = []
+    for d in (big, med):
+        nd = lens[d] // 2
+        nbd = nd // B
+        blocks += [(d, 0), (d, B), (d, (nbd // 2) * B), (d, nd - B), (d, nd), (d, nd + (nbd // 2) * B),
+                   (d, 2 * nd - 2 * B), (d, 2 * nd - B)]
+    sm = slice(cu[med], cu[med + 1])
+    for g in range(w.kv_heads):
+        sampled_rows_check(x, w, o, lse, dq, kv_groups=[g], blocks=blocks, cu=cu)
+        q, k, v, do = (f32(t[sm]) for t in group_slices(x, w, g))
+        r = oracle.bdlm_attention(q, k, v, B, w.scale, do=do)
+        hs = slice(g * G, (g + 1) * G)
+        tag = f"median document, kv group {g}"
+        check_o(host(o[sm][:, hs]), r["o"], "o, " + tag)
+        check_lse(host(lse[hs, sm]), r["lse"], "lse, " + tag)
+        check_grad(host(dq[sm][:, hs]), r["dq"], "dq, " + tag)
+        check_grad(host(dk[sm][:, g:g + 1]), r["dk"], "dk, " + tag)
+        check_grad(host(dv[sm][:, g:g + 1]), r["dv"], "dv, " + tag)
     identities_check(x, w, dk, dv)
 
 
