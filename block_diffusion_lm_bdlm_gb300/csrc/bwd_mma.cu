@@ -17,6 +17,7 @@
 //   3. convert: dq = bf16(accumulator), times the softmax scale when the
 //      main kernel accumulated dS K unscaled (the tensor-core kernel).
 #include <climits>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -307,8 +308,12 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if constexpr (D == 128) {
+    const char* kv = getenv("BDLM_BWD_K");
+    const bool old = kv && kv[0] == 'o';
+    if (!old) {
         e = launch_bwd_tc_main(a, num_sms, st);  // tensor-core main kernel, 128-key tiles
+    } else if constexpr (D == 128) {
+        e = launch_bwd_tc64_main(a, num_sms, st);
     } else {
         constexpr int smem = bwd_smem_bytes<D>();
         e = cudaFuncSetAttribute(bwd_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -318,7 +323,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
     }
     if (e != cudaSuccess) return e;
     const long long cv = pairs * D / 8;
-    bwd_convert_kernel<D><<<(unsigned)((cv + 255) / 256), 256, 0, st>>>(a, D == 128 ? a.scale : 1.f);
+    bwd_convert_kernel<D><<<(unsigned)((cv + 255) / 256), 256, 0, st>>>(a, (!old || D == 128) ? a.scale : 1.f);
     return cudaGetLastError();
 }
 

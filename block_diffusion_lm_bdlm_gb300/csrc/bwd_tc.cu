@@ -1,48 +1,59 @@
 // bwd_tc.cu - BDLM attention backward main kernel on the 5th-generation
-// tensor cores (head_dim 128).
+// tensor cores (head_dim 64 and 128).
 //
 // Key-major: one work item = (128-key tile, kv head). The item loops over the
-// G query heads of the kv head and, for each, over the 64-row query steps
+// G query heads of the kv head and, for each, over the 128-row query steps
 // that see the key tile (a clean key tile is seen by the clean rows from its
 // block on and by the corrupted rows of later blocks; a corrupted key tile
-// only by its own blocks' corrupted rows). Per step:
-//   S^T  = K Q^T          (M 128 keys, N 64 rows, K = d)      -> TMEM
-//   dP^T = V dO^T                                              -> TMEM
-//   P^T  = exp2(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D)
-//          (compute warps; P^T and dS^T go to their own TMEM columns as bf16
-//          for dV and dK, and dS^T also to shared memory for dQ^T)
-//   dV  += P^T dO         (A from TMEM)                        -> TMEM
-//   dK  += dS^T Q         (A from TMEM)                        -> TMEM
-//   dQ^T = K^T dS^T       (M = d, N 64 rows, K 128 keys)       -> TMEM
-//          read out, scaled, staged in shared memory and added into the fp32
-//          dq accumulator with one TMA reduce-add per step.
+// only by its own blocks' corrupted rows). Per step, every product is a
+// 128 x 128 tensor-core tile, the shape at which tcgen05.mma runs at its full
+// rate (a 64-wide B operand costs more shared-memory reads than the MMA has
+// cycles):
+//   S^T  = K Q^T          (M 128 keys, N 128 rows, K = d)          -> RS
+//   dP^T = V dO^T                                                   -> RP
+//   P^T  = exp2(S^T*scale*log2e - lse*log2e)   (compute warps; bf16 P^T
+//          written over the S^T columns it came from)
+//   dS^T = P^T (dP^T - D)  (bf16, over the dP^T columns, and to shared memory)
+//   dV  += P^T dO         (A from TMEM)                             -> TMEM
+//   dK  += dS^T Q         (A from TMEM)                             -> TMEM
+//   d 128: dQ^T = K^T dS^T (M = d, N 128 rows, K 128 keys)           -> RP
+//   d 64:  dQ   = dS K     (M 128 rows, N = d, K 128 keys)           -> own columns
+//          read out and added into the fp32 dq accumulator from registers
+//          (unscaled; the convert kernel applies the softmax scale).
 // dK and dV stay in TMEM for the whole item (no atomics: the item owns its
 // keys for all G heads) and are written once, as bf16, at the end.
 //
-// Warp roles (448 threads):
+// TMEM (512 columns): dK [0, d) | dV [d, 2d) | (d 64: dQ [128, 192)) |
+// RS [256, 384) | RP [384, 512). The tensor pipe runs one CTA's MMAs in issue
+// order, so an MMA may overwrite columns that an earlier-issued MMA reads:
+// S^T(s+1) goes into RS right after dV(s) (which reads P^T(s) there), and for
+// d 128 dQ^T(s) goes into RP right after dK(s) (which reads dS^T(s) there).
+// Per step s the tensor pipe receives, in this order:
+//   dP^T(s)  [RP free: dQ^T(s-1) read out]
+//   dV(s)    [P^T(s) stored]
+//   S^T(s+1) [Q(s+1) loaded]
+//   dK(s)    [dS^T(s) stored]
+//   dQ(s)    [d 64: dQ(s-1) read out]
+// so that the compute warps work on P(s+1) while dK(s) and dQ(s) run, and on
+// dS(s) while dV(s) and S^T(s+1) run.
+//
+// Warp roles (512 threads):
 //   warps 0-7   P/dS groups: one TMEM lane = one key row; group g (warps
-//               4g..4g+3) takes query columns 32g..32g+31 of a step. The mask
+//               4g..4g+3) takes query columns 64g..64g+63 of a step. The mask
 //               is analytic: for one key, the rows of a step that see it form
 //               one interval (later clean blocks / later corrupted blocks for a
 //               clean key, its own corrupted block for a corrupted key).
-//   warps 8-11  dq group: reads dQ^T (lane = d) out to the TMA reduce-add
-//               through a double-buffered staging tile, and writes dK and dV
-//               at the end of an item
-//   warp  12    loader: TMA for K, V, Q, dO; plain loads for lse and D; 3-stage
-//               ring for the per-step inputs
-//   warp  13    TMEM owner and MMA issuer (one thread). Per step s it issues
-//              S^T(s+1) and dP^T(s+1) as soon as the P/dS warps have read
-//              S^T(s) and dP^T(s) out of TMEM, then dV(s) and dK(s) once
-//              P/dS(s) is done, then dQ^T(s): the next step's S^T and dP^T run
-//              on the tensor pipe while P/dS(s) computes.
-// TMEM columns: dK [0,128) | dV [128,256) | S^T [256,320) | dP^T [320,384) |
-// P^T [384,416) | dQ^T [416,480) | dS^T [480,512). dS^T in shared memory is
-// double buffered. Because P^T and dS^T do not alias S^T and dP^T, S^T and
-// dP^T are free once loaded (barrier B_LD); P^T and dS^T of step s+1 are
-// written only after dV(s) and dK(s) completed (the stage's B_QDE commit).
-// The shared-memory copy of dS^T has its own barrier, needed only by dQ^T;
-// tcgen05 commit order covers the rest (an MMA's commit also covers every MMA
-// issued before it).
+//               Group g writes its bf16 P^T and dS^T halves into its own
+//               fp32 columns (RS / RP + 64g), so neither group overwrites
+//               columns the other has not read yet.
+//   warps 8-11  dq group: reads dQ^T (d 128: lane = d) or dQ (d 64: lane =
+//               row) out of TMEM and reduces it into the fp32 dq accumulator;
+//               writes dK and dV at the end of an item
+//   warp  12    loader: TMA for K, V, Q, dO; plain loads for lse and D; two
+//               stages for the per-step inputs
+//   warp  13    TMEM owner and MMA issuer (one thread)
+//   warps 14-15 idle: they complete the loader/MMA warpgroup, whose
+//               registers setmaxnreg hands to the other roles
 // Every mbarrier wait is bounded (2 s).
 #include <cuda.h>
 
@@ -53,38 +64,59 @@
 namespace bdlm {
 namespace {
 
-constexpr int D = 128;
 constexpr int BN = 128;  // keys per item
-constexpr int BQ = 64;   // query rows per step
-constexpr int kThreads = 448;
+constexpr int BQ = 128;  // query rows per step
+constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kStages = 2;
 
-constexpr uint32_t TDK = 0, TDV = 128, TS = 256, TDP = 320, TP = 384, TDQ = 416, TDS = 480;
-constexpr int kStages = 3;
+constexpr uint32_t TRS = 256, TRP = 384;
 
-// dynamic shared memory (1024-aligned offsets)
-constexpr int kKV = BN * D * 2;     // 32 KB: K or V tile, two 64-column chunks of 16 KB
-constexpr int kQT = BQ * D * 2;     // 16 KB: Q or dO tile, two chunks of 8 KB
-constexpr int kST = BN * BQ * 2;    // 16 KB: dS^T [128 keys][64 rows] bf16, 128-byte swizzled rows
-constexpr int kHalfRows = BQ / 2;   // dq staging holds half a step: [32 rows][128] fp32
-constexpr int SM_K = 0;
-constexpr int SM_V = SM_K + kKV;
-constexpr int SM_Q = SM_V + kKV;                // + stage * kQT
-constexpr int SM_O = SM_Q + kStages * kQT;      // + stage * kQT
-constexpr int SM_S = SM_O + kStages * kQT;      // + buffer * kST
-constexpr int kStg = kHalfRows * D * 4;  // 16 KB per staging buffer
-constexpr int SM_STG = SM_S + 2 * kST;     // + buffer * kStg
-constexpr int kSmemBytes = SM_STG + 2 * kStg + 1024;
+// Registers per thread: the launch gives every warp 128 (16 warps, 4 on each
+// SM sub-partition of 512 per lane). setmaxnreg moves them between whole
+// warpgroups: the loader/MMA warpgroup (warps 12-15, two of them idle) gives
+// half of its share to the P/dS warpgroups and to the dq warpgroup, which
+// holds a whole step of dQ^T (128 values) while it reduces it:
+// 8 x 144 + 4 x 160 + 4 x 64 = 16 x 128, and per sub-partition (warps w,
+// w+4, w+8, w+12) 144 + 144 + 160 + 64 = 512.
+constexpr int kRegsPds = 144;
+constexpr int kRegsDq = 160;
+constexpr int kRegsIo = 64;
 
 enum : int {
-    B_KV = 0, B_QDF = 1, B_QDE = 4, B_S = 7, B_DP = 8, B_SM = 9, B_SS = 10 /* x2, by step parity */, B_DQ = 12, B_DQF = 13,
-    B_LD = 14, B_COUNT = 15
+    B_KV = 0, B_QF = 1 /* x2 */, B_QE = 3 /* x2 */, B_OF = 5 /* x2 */, B_OE = 7 /* x2 */, B_S = 9, B_DP = 10,
+    B_P = 11, B_DS = 12, B_DSS = 13, B_DQ = 14, B_DQF = 15, B_SF = 16, B_COUNT = 17
 };
 
 struct StepInfo {
     float nl2[BQ];   // -lse * log2(e) of the step's rows (0 beyond the step; those rows are masked)
     float dsum[BQ];  // D = rowsum(dO * o)
+};
+
+// Shared memory (offsets from a 1024-byte aligned base). Operand tiles are
+// 128-byte swizzled [rows][64 columns] chunks of 16 KB.
+template <int D>
+struct Smem {
+    static constexpr int kChunk = 128 * 128;           // [128 rows][64 bf16]
+    static constexpr int kKV = BN * D * 2;             // K or V tile: D / 64 chunks
+    static constexpr int kQT = BQ * D * 2;             // Q or dO tile: D / 64 chunks
+    static constexpr int kST = BN * BQ * 2;            // dS^T [128 keys][128 rows]: 2 chunks of 64 rows
+    static constexpr int K = 0;
+    static constexpr int V = K + kKV;
+    static constexpr int Q = V + kKV;                  // + stage * kQT
+    static constexpr int O = Q + kStages * kQT;        // + stage * kQT
+    static constexpr int S = O + kStages * kQT;
+    static constexpr int INFO = S + kST;               // StepInfo[kStages]
+    static constexpr int BAR = INFO + kStages * (int)sizeof(StepInfo);
+    static constexpr int MISC = BAR + B_COUNT * 8;     // TMEM address, item, abort flag
+    static constexpr int kBytes = MISC + 16;
+};
+static_assert(Smem<128>::kBytes <= 227 * 1024, "shared memory of the d 128 backward");
+
+template <int D>
+struct Tm {
+    static constexpr uint32_t DK = 0, DV = D, DQ = 128;  // DQ: d 64 only
 };
 
 struct ItemCtx {
@@ -106,6 +138,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void named_sync_all() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void named_sync_dq() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
     asm volatile(
         "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
@@ -113,29 +147,21 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-// Barrier over the n threads of named barrier `id` that also ANDs a predicate,
-// so that a decision to stop is taken by all of them together.
-__device__ __forceinline__ bool named_and(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
+__device__ __forceinline__ void red_add_v4f32(float* p, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
 }
 
 // Item -> (key tile, kv head). Tiles are ordered heaviest first. By default
 // (K = 1) the items of one tile (its kv heads) are consecutive, so the order
 // is strictly heaviest first. For packed documents with many tiles the items
 // go in blocks of K = gridDim.x / 2 tiles, kv head by kv head within a block
-// (one wave of gridDim.x items spans two kv heads): measured on a GB300, this
-// takes the 64-document packed backward from 93.3 to 85.1 ms, while single
-// long sequences ran about 1 % faster with K = 1 (their DRAM traffic drops
-// about 4x with the blocks, but they are not bound by it).
+// (one wave of gridDim.x items spans two kv heads), which keeps the query
+// rows a wave sweeps within two kv heads' worth of L2.
 __device__ __forceinline__ ItemCtx decode(const BwdArgs& a, int item) {
     ItemCtx c;
     const int nt = a.hdr->n_tiles;
@@ -159,7 +185,7 @@ __device__ __forceinline__ ItemCtx decode(const BwdArgs& a, int item) {
     return c;
 }
 
-// query rows of step s: head, first document position, valid rows
+// query rows of step s: head, first row position, valid rows
 __device__ __forceinline__ void step_rows(const ItemCtx& c, const BwdArgs& a, int s, int* h, int* p0, int* nrows) {
     const int hh = s / c.per_head, rem = s % c.per_head;
     *h = c.kvh * a.G + hh;
@@ -169,40 +195,45 @@ __device__ __forceinline__ void step_rows(const ItemCtx& c, const BwdArgs& a, in
 }
 
 // ---------------------------------------------------------------- loader
+template <int D>
 __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, const uint64_t* bar,
                                           StepInfo* info, const CUtensorMap* tk, const CUtensorMap* tv,
                                           const CUtensorMap* tq, const CUtensorMap* tdo, uint32_t ts_base,
                                           volatile int* abort) {
+    using L = Smem<D>;
+    constexpr int NC = D / 64;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         const uint32_t bkv = tc::smem_addr(&bar[B_KV]);
-        tc::mbar_arrive_expect_tx(bkv, 2 * kKV);
-        for (int ch = 0; ch < 2; ++ch) {
-            tc::tma_load_3d(sbase + SM_K + ch * (kKV / 2), tk, bkv, 64 * ch, c.kvh, c.k0);
-            tc::tma_load_3d(sbase + SM_V + ch * (kKV / 2), tv, bkv, 64 * ch, c.kvh, c.k0);
+        tc::mbar_arrive_expect_tx(bkv, 2 * L::kKV);
+        for (int ch = 0; ch < NC; ++ch) {
+            tc::tma_load_3d(sbase + L::K + ch * L::kChunk, tk, bkv, 64 * ch, c.kvh, c.k0);
+            tc::tma_load_3d(sbase + L::V + ch * L::kChunk, tv, bkv, 64 * ch, c.kvh, c.k0);
         }
     }
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages, ph = (ts / kStages) & 1;
-        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + st]), ph ^ 1, abort, kTimeoutNs);
+        // Q stage (with the step's lse and D): free once dK two steps back
+        // has read it. dO stage: for d 128, once the dq warps' staging of two
+        // steps back has been reduced out of it; for d 64, with the Q stage.
+        // Each tile goes as soon as its own stage is free.
+        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QE + st]), ph ^ 1, abort, kTimeoutNs);
         if (!__all_sync(0xffffffffu, got)) return;
         int h, p0, nrows;
         step_rows(c, a, s, &h, &p0, &nrows);
         const int qr0 = q_row_of(a.lay, c.kt, p0);
-        const uint32_t bf = tc::smem_addr(&bar[B_QDF + st]);
+        const uint32_t bf = tc::smem_addr(&bar[B_QF + st]);
         if (lane == 0) {
-            mbar_expect_tx(bf, 2 * kQT);
-            for (int ch = 0; ch < 2; ++ch) {
-                tc::tma_load_3d(sbase + SM_Q + st * kQT + ch * (kQT / 2), tq, bf, 64 * ch, h, qr0);
-                tc::tma_load_3d(sbase + SM_O + st * kQT + ch * (kQT / 2), tdo, bf, 64 * ch, h, qr0);
-            }
+            mbar_expect_tx(bf, L::kQT);
+            for (int ch = 0; ch < NC; ++ch)
+                tc::tma_load_3d(sbase + L::Q + st * L::kQT + ch * L::kChunk, tq, bf, 64 * ch, h, qr0);
         }
-        // lse and D: plain loads (the loader runs steps ahead of the MMAs),
+        // lse and D: plain loads (the loader runs a step ahead of the MMAs),
         // stored pre-scaled so that P/dS spends one FFMA per element before exp2
         StepInfo& inf = info[st];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int r = 2 * lane + u;
+        for (int u = 0; u < BQ / 32; ++u) {
+            const int r = (BQ / 32) * lane + u;
             float nl2 = 0.f, dd = 0.f;
             if (r < nrows) {
                 const long long gi = (long long)h * a.Lq + qr0 + r;
@@ -213,6 +244,14 @@ __device__ __forceinline__ void load_item(const ItemCtx& c, const BwdArgs& a, ui
             inf.dsum[r] = dd;
         }
         tc::mbar_arrive(bf);
+        if (D == 128) got = tc::mbar_wait(tc::smem_addr(&bar[B_OE + st]), ph ^ 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) return;
+        if (lane == 0) {
+            const uint32_t bo = tc::smem_addr(&bar[B_OF + st]);
+            tc::mbar_arrive_expect_tx(bo, L::kQT);
+            for (int ch = 0; ch < NC; ++ch)
+                tc::tma_load_3d(sbase + L::O + st * L::kQT + ch * L::kChunk, tdo, bo, 64 * ch, h, qr0);
+        }
     }
 }
 
@@ -223,109 +262,119 @@ __device__ __forceinline__ bool mma_wait(const uint64_t* bar, int i, uint32_t pa
     return true;
 }
 
-// Shared-memory descriptors of the operand tiles at stage / buffer 0; the MMA
-// thread steps to K slices, stages and buffers with tc::sdesc_add instead of
-// rebuilding descriptors.
+// Shared-memory descriptors of the operand tiles at stage 0; the MMA thread
+// steps to K slices and stages with tc::sdesc_add.
+template <int D>
 struct Descs {
     uint64_t k_km, v_km, q_km, o_km;  // K-major (S^T, dP^T operands)
-    uint64_t k_mn, s_mn, q_mn, o_mn;  // MN-major (dQ^T, dK, dV operands)
+    uint64_t k_mn, s_mn, q_mn, o_mn;  // MN-major (dQ, dK, dV operands)
+    __device__ __forceinline__ explicit Descs(uint32_t sbase) {
+        using L = Smem<D>;
+        k_km = tc::sdesc_sw128(sbase + L::K, 16, 1024);
+        v_km = tc::sdesc_sw128(sbase + L::V, 16, 1024);
+        q_km = tc::sdesc_sw128(sbase + L::Q, 16, 1024);
+        o_km = tc::sdesc_sw128(sbase + L::O, 16, 1024);
+        k_mn = tc::sdesc_sw128(sbase + L::K, L::kChunk, 1024);
+        s_mn = tc::sdesc_sw128(sbase + L::S, L::kChunk, 1024);
+        q_mn = tc::sdesc_sw128(sbase + L::Q, L::kChunk, 1024);
+        o_mn = tc::sdesc_sw128(sbase + L::O, L::kChunk, 1024);
+    }
 };
-__device__ __forceinline__ Descs make_descs(uint32_t sbase) {
-    Descs d;
-    d.k_km = tc::sdesc_sw128(sbase + SM_K, 16, 1024);
-    d.v_km = tc::sdesc_sw128(sbase + SM_V, 16, 1024);
-    d.q_km = tc::sdesc_sw128(sbase + SM_Q, 16, 1024);
-    d.o_km = tc::sdesc_sw128(sbase + SM_O, 16, 1024);
-    d.k_mn = tc::sdesc_sw128(sbase + SM_K, kKV / 2, 1024);
-    d.s_mn = tc::sdesc_sw128(sbase + SM_S, kKV / 2, 1024);
-    d.q_mn = tc::sdesc_sw128(sbase + SM_Q, kQT / 2, 1024);
-    d.o_mn = tc::sdesc_sw128(sbase + SM_O, kQT / 2, 1024);
-    return d;
-}
 __device__ __forceinline__ uint64_t at(uint64_t desc, uint32_t bytes) { return tc::sdesc_add(desc, bytes); }
 
-__device__ __forceinline__ bool issue_dq(const Descs& dd, const uint64_t* bar, uint32_t tmem, uint32_t ts, int s,
-                                         volatile int* abort) {
-    constexpr uint32_t id_dq = tc::idesc_bf16(D, BQ, 1) | (1u << 15);  // A and B MN-major
-    // dQ^T of the previous step must have been read out of TMEM, and this
-    // step's dS^T must be in shared memory (one barrier per step parity: the
-    // P/dS warps cannot get two steps ahead, the step after next needs a
-    // dP^T that is issued after this dQ^T)
-    if (s >= 1 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) return false;
-    if (!mma_wait(bar, B_SS + (ts & 1), (ts >> 1) & 1, abort)) return false;
-    const uint64_t sS = at(dd.s_mn, (ts & 1) * kST);
-#pragma unroll
-    for (int k = 0; k < BN / 16; ++k) tc::mma_ss(tmem + TDQ, at(dd.k_mn, 2048 * k), at(sS, 2048 * k), id_dq, k > 0);
-    tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
-    return true;
-}
-
-// S^T = K Q^T and dP^T = V dO^T of global step ts, once its Q and dO are in shared memory.
-__device__ __forceinline__ bool issue_sdp(const Descs& dd, const uint64_t* bar, uint32_t tmem, uint32_t ts,
-                                          volatile int* abort) {
-    constexpr uint32_t id_st = tc::idesc_bf16(BN, BQ, 0);  // A, B K-major
-    const uint32_t st = ts % kStages;
-    if (!mma_wait(bar, B_QDF + st, (ts / kStages) & 1, abort)) return false;
-    const uint64_t q = at(dd.q_km, st * kQT), o = at(dd.o_km, st * kQT);
+// A[keys, K = d] x B[rows, K = d]^T into the 128 x 128 fp32 columns at dst
+// (S^T from K and Q, dP^T from V and dO), both operands K-major.
+template <int D>
+__device__ __forceinline__ void mma_kq(uint32_t dst, uint64_t a, uint64_t b) {
+    constexpr uint32_t id = tc::idesc_bf16(BN, BQ, 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-        const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-        tc::mma_ss(tmem + TS, at(dd.k_km, oa), at(q, ob), id_st, k > 0);
+        const uint32_t off = (k >> 2) * Smem<D>::kChunk + (k & 3) * 32;
+        tc::mma_ss(dst, at(a, off), at(b, off), id, k > 0);
     }
-    tc::mma_commit(tc::smem_addr(&bar[B_S]));
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-        const uint32_t oa = (k >> 2) * (kKV / 2) + (k & 3) * 32, ob = (k >> 2) * (kQT / 2) + (k & 3) * 32;
-        tc::mma_ss(tmem + TDP, at(dd.v_km, oa), at(o, ob), id_st, k > 0);
-    }
-    tc::mma_commit(tc::smem_addr(&bar[B_DP]));
-    return true;
 }
 
-// Per step s the tensor pipe receives S^T(s+1), dP^T(s+1), dV(s), dK(s),
-// dQ^T(s): the next step's S^T and dP^T go in as soon as the P/dS warps have
-// read S^T(s) and dP^T(s) into registers (B_LD), so they run while P/dS(s) is
-// still computing; dV(s) and dK(s) wait for P^T(s) and dS^T(s) (B_SM).
+// The columns of group g's K slices of a bf16 operand written over fp32
+// columns (P^T over RS, dS^T over RP): slice k (rows 16k..16k+15 of the step)
+// belongs to group k / 4 and sits at base + 64 (k / 4) + 8 (k % 4).
+__device__ __forceinline__ uint32_t slice_col(int k) { return 64u * (uint32_t)(k >> 2) + 8u * (uint32_t)(k & 3); }
+
+template <int D>
 __device__ __forceinline__ void issue_item(const ItemCtx& c, uint32_t sbase, const uint64_t* bar, uint32_t tmem,
                                            uint32_t ts_base, uint32_t item_count, volatile int* abort) {
-    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);  // dV, dK: A K-major (TMEM), B MN-major
+    using L = Smem<D>;
+    using T = Tm<D>;
+    constexpr uint32_t id_kv = tc::idesc_bf16(BN, D, 1);                 // dV, dK: A from TMEM, B MN-major
+    constexpr uint32_t id_dq = D == 128 ? tc::idesc_bf16(D, BQ, 1) | (1u << 15)   // dQ^T: A, B MN-major
+                                        : tc::idesc_bf16(BQ, D, 1) | (1u << 15);  // dQ:   A, B MN-major
     if (!mma_wait(bar, B_KV, item_count & 1, abort)) return;
     if (c.n_steps == 0) return;
-    const Descs dd = make_descs(sbase);
-    if (!issue_sdp(dd, bar, tmem, ts_base, abort)) return;
+    const Descs<D> dd(sbase);
+    {   // S^T of the item's first step
+        const uint32_t st = ts_base % kStages;
+        if (!mma_wait(bar, B_QF + st, (ts_base / kStages) & 1, abort)) return;
+        mma_kq<D>(tmem + TRS, dd.k_km, at(dd.q_km, st * L::kQT));
+        tc::mma_commit(tc::smem_addr(&bar[B_S]));
+    }
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
+        // dP^T(s) into RP (for d 128, RP last held dQ^T(s-1)), once dO(s) is in
+        if (D == 128 && ts > 0 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) return;
+        if (!mma_wait(bar, B_OF + st, (ts / kStages) & 1, abort)) return;
+        mma_kq<D>(tmem + TRP, dd.v_km, at(dd.o_km, st * L::kQT));
+        tc::mma_commit(tc::smem_addr(&bar[B_DP]));
+        // dV += P^T dO
+        if (!mma_wait(bar, B_P, ts & 1, abort)) return;
+        const uint64_t o = at(dd.o_mn, st * L::kQT), q = at(dd.q_mn, st * L::kQT);
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+            tc::mma_ts(tmem + T::DV, tmem + TRS + slice_col(k), at(o, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
+        // S^T(s+1) into RS (after dV(s) in the pipe, which read P^T(s) there)
         if (s + 1 < c.n_steps) {
-            if (!mma_wait(bar, B_LD, ts & 1, abort)) return;
-            if (!issue_sdp(dd, bar, tmem, ts + 1, abort)) return;
+            const uint32_t tn = ts + 1, sn = tn % kStages;
+            if (!mma_wait(bar, B_QF + sn, (tn / kStages) & 1, abort)) return;
+            mma_kq<D>(tmem + TRS, dd.k_km, at(dd.q_km, sn * L::kQT));
+            tc::mma_commit(tc::smem_addr(&bar[B_S]));
         }
-        if (!mma_wait(bar, B_SM, ts & 1, abort)) return;
-        // dV += P^T dO, dK += dS^T Q (P^T and dS^T in TMEM)
-        const uint64_t q = at(dd.q_mn, st * kQT), o = at(dd.o_mn, st * kQT);
+        // dK += dS^T Q
+        if (!mma_wait(bar, B_DS, ts & 1, abort)) return;
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDV, tmem + TP + 8 * k, at(o, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(tmem + T::DK, tmem + TRP + slice_col(k), at(q, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(tc::smem_addr(&bar[B_QE + st]));  // Q(s) (and dO(s)) read by every MMA that needs them
+        // dq of this step from dS^T in shared memory and the K tile
+        if (!mma_wait(bar, B_DSS, ts & 1, abort)) return;
+        if (D == 128) {  // dQ^T = K^T dS^T into RP (after dK(s) in the pipe, which read dS^T(s) there)
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
-            tc::mma_ts(tmem + TDK, tmem + TDS + 8 * k, at(q, 2048 * k), id_kv, (s > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(tc::smem_addr(&bar[B_QDE + st]));
-        if (!issue_dq(dd, bar, tmem, ts, s, abort)) return;
+            for (int k = 0; k < BN / 16; ++k)
+                tc::mma_ss(tmem + TRP, at(dd.k_mn, 2048 * k), at(dd.s_mn, 2048 * k), id_dq, k > 0);
+        } else {         // dQ = dS K into its own columns, once dQ(s-1) has been read out
+            if (ts > 0 && !mma_wait(bar, B_DQF, (ts - 1) & 1, abort)) return;
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+                tc::mma_ss(tmem + T::DQ, at(dd.s_mn, 2048 * k), at(dd.k_mn, 2048 * k), id_dq, k > 0);
+        }
+        tc::mma_commit(tc::smem_addr(&bar[B_DQ]));
     }
 }
 
 // ------------------------------------------------------------ P/dS group
-// Thread = one key row (TMEM lane) x query columns 32g .. 32g + 31.
+// Thread = one key row (TMEM lane) x query columns 64g .. 64g + 63.
+template <int D>
 __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uint8_t* smem, const uint64_t* bar,
                                          const StepInfo* info, uint32_t tmem, uint32_t ts_base, volatile int* abort) {
+    using L = Smem<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = warp >> 2;
     const int kk = 32 * (warp & 3) + lane;  // key row in the tile == TMEM lane
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-    const float sl2 = a.scale_log2;
+    const uint32_t tS = tmem + lb + TRS + 64 * g, tP = tmem + lb + TRP + 64 * g;
+    const float2 sl2x2 = make_float2(a.scale_log2, a.scale_log2);
     // Row positions that see this thread's key, one interval per query range:
     // a clean key of block b is seen by clean rows of blocks >= b and corrupted
     // rows of blocks > b; a corrupted key only by the corrupted rows of its block.
     const KeyRows kr = key_rows(a.lay, c.kt, kk);
+    uint8_t* srow = smem + L::S + g * L::kChunk + kk * 128;  // this thread's row of dS^T, chunk g
     int rem = 0;  // step index within the current query head
     for (int s = 0; s < c.n_steps; ++s) {
         const uint32_t ts = ts_base + s, st = ts % kStages;
@@ -333,112 +382,186 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         const int p0 = in_a ? c.ra_lo + rem * BQ : c.rb_lo + (rem - c.na) * BQ;
         const int nrows = imin(BQ, (in_a ? c.ra_hi : c.rb_hi) - p0);
         if (++rem == c.per_head) rem = 0;
-        const int lo = imax((in_a ? kr.a_lo : kr.b_lo) - p0, 0) - 32 * g;  // relative to this group's first column
-        const int hi = imin((in_a ? kr.a_hi : kr.b_hi) - p0, nrows) - 32 * g;
+        const int lo = imax((in_a ? kr.a_lo : kr.b_lo) - p0, 0) - 64 * g;  // relative to this group's first column
+        const int hi = imin((in_a ? kr.a_hi : kr.b_hi) - p0, nrows) - 64 * g;
         const int len = imax(hi - lo, 0);
-        const bool all_visible = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
-        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QDF + st]), (ts / kStages) & 1, abort, kTimeoutNs);
+        const bool all_visible = __all_sync(0xffffffffu, lo <= 0 && hi >= 64);
+        // ---- P^T = exp2(S^T scale log2e - lse log2e), masked; bf16 over RS + 64g
+        bool got = tc::mbar_wait(tc::smem_addr(&bar[B_QF + st]), (ts / kStages) & 1, abort, kTimeoutNs);
         got = got && tc::mbar_wait(tc::smem_addr(&bar[B_S]), ts & 1, abort, kTimeoutNs);
-        got = got && tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
         if (!__all_sync(0xffffffffu, got)) return;
         tc::tc_fence_after();
-        uint32_t sr[32], dr[32];
-        tc::tmem_ld32(tmem + lb + TS + 32 * g, sr);
-        tc::tmem_ld32(tmem + lb + TDP + 32 * g, dr);
-        const float4* lse4 = reinterpret_cast<const float4*>(info[st].nl2 + 32 * g);
-        const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 32 * g);
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_LD]));  // S^T and dP^T of the next step may go
-        uint32_t pp[16], dd[16];
-        const float2 sl2x2 = make_float2(sl2, sl2);
+        float p[64];
+        {
+            uint32_t r0[32], r1[32];
+            tc::tmem_ld32(tS, r0);
+            tc::tmem_ld32(tS + 32, r1);
+            tc::tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 l4 = lse4[q], d4 = ds4[q];
+            for (int e = 0; e < 32; ++e) {
+                p[e] = __uint_as_float(r0[e]);
+                p[32 + e] = __uint_as_float(r1[e]);
+            }
+        }
+        const float4* nl4 = reinterpret_cast<const float4*>(info[st].nl2 + 64 * g);
+        uint32_t pk[32];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 l4 = nl4[q];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int col = 4 * q + 2 * u;
                 const float2 nl = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
-                const float2 dsum = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-                const float2 x = tc::fma2(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sl2x2, nl);
-                float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+                const float2 x = tc::fma2(make_float2(p[col], p[col + 1]), sl2x2, nl);
+                float2 e2 = make_float2(ex2f(x.x), ex2f(x.y));
                 if (!all_visible) {
-                    p.x = (unsigned)(col - lo) < (unsigned)len ? p.x : 0.f;
-                    p.y = (unsigned)(col + 1 - lo) < (unsigned)len ? p.y : 0.f;
+                    e2.x = (unsigned)(col - lo) < (unsigned)len ? e2.x : 0.f;
+                    e2.y = (unsigned)(col + 1 - lo) < (unsigned)len ? e2.y : 0.f;
                 }
-                const float2 ds = tc::mul2(p, tc::sub2(make_float2(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), dsum));
-                pp[2 * q + u] = pack2(p.x, p.y);
-                dd[2 * q + u] = pack2(ds.x, ds.y);
+                p[col] = e2.x;
+                p[col + 1] = e2.y;
+                pk[2 * q + u] = pack2(e2.x, e2.y);
             }
         }
-        // P^T and dS^T of the previous step must have been read by its dV and dK
-        if (ts > 0) {
-            const uint32_t tp = ts - 1;
-            got = tc::mbar_wait(tc::smem_addr(&bar[B_QDE + tp % kStages]), (tp / kStages) & 1, abort, kTimeoutNs);
-            if (!__all_sync(0xffffffffu, got)) return;
-            tc::tc_fence_after();
-        }
-        tc::tmem_st16(tmem + lb + TP + 16 * g, pp);
-        tc::tmem_st16(tmem + lb + TDS + 16 * g, dd);
+        tc::tmem_st32(tS, pk);
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_SM]));  // dV and dK may go
-        {   // dS^T row kk, columns 32g..32g+31 = 16-byte chunks 4g..4g+3 of a 128-byte swizzled row
-            uint8_t* srow = smem + SM_S + (ts & 1) * kST + kk * 128;
+        tc::mbar_arrive(tc::smem_addr(&bar[B_P]));  // dV(s) and then S^T(s+1) may go
+        // ---- dS^T = P^T (dP^T - D), bf16 over RP + 64g (for dK), then into
+        // shared memory (for dQ)
+        got = tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) return;
+        tc::tc_fence_after();
+        const float4* ds4 = reinterpret_cast<const float4*>(info[st].dsum + 64 * g);
+        uint32_t dk[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int chunk = (4 * g + q) ^ (kk & 7);
-                *reinterpret_cast<uint4*>(srow + chunk * 16) = make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+        for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            tc::tmem_ld32(tP + 32 * half, r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 d4 = ds4[8 * half + q];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = 4 * q + 2 * u, col = 32 * half + e;
+                    const float2 dsum = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                    const float2 ds = tc::mul2(make_float2(p[col], p[col + 1]),
+                                               tc::sub2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), dsum));
+                    dk[16 * half + 2 * q + u] = pack2(ds.x, ds.y);
+                }
             }
         }
+        tc::tmem_st32(tP, dk);
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_addr(&bar[B_DS]));  // dK(s) may go
+        // the shared-memory dS^T buffer is free: d 128, the dq warps' staging
+        // of step s-1 has been reduced out of it; d 64, dQ(s-1) has read it
+        got = ts == 0 || tc::mbar_wait(tc::smem_addr(&bar[D == 128 ? B_SF : B_DQ]), (ts - 1) & 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) return;
+        // row kk of dS^T chunk g: eight 16-byte units, 128-byte swizzled
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int unit = q ^ (kk & 7);
+            *reinterpret_cast<uint4*>(srow + unit * 16) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+        }
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_SS + (ts & 1)]));  // dQ^T may go (issued one step later)
+        tc::mbar_arrive(tc::smem_addr(&bar[B_DSS]));  // dQ(s) may go
     }
 }
 
 // -------------------------------------------------------------- dq group
-// Thread = one head-dim lane d of dQ^T (TMEM lane) x 64 query columns; the
-// step's dq goes out as two TMA reduce-adds of 32 rows through two staging
-// buffers. At the end of the item it writes dK and dV (thread = key row).
-__device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint32_t sbase, uint8_t* smem,
+// d 128: thread = one head-dim lane d of dQ^T (TMEM lane) x the step's 128
+// query columns; a warp's 32 lanes reduce 32 consecutive d of one row (128
+// contiguous bytes) per instruction. d 64: thread = one query row of dQ x 64
+// d; 16-byte vector reductions. At the end of the item it writes dK and dV
+// (thread = key row).
+// (The step loop keeps only the few values it needs live; the item is
+// decoded again for the dK, dV epilogue, which keeps the dq warps within
+// their register budget while they hold a whole step of dQ^T.)
+template <int D>
+__device__ __forceinline__ bool dq_item(int item, int n_steps, const BwdArgs& a, uint8_t* smem, uint32_t sbase,
                                         const uint64_t* bar, uint32_t tmem, const CUtensorMap* tdq, uint32_t ts_base,
                                         volatile int* abort) {
+    using T = Tm<D>;
+    using L = Smem<D>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int dl = 32 * (warp & 3) + lane;  // d index == TMEM lane
+    const int dl = 32 * (warp & 3) + lane;  // TMEM lane
     const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-    const bool leader = tid == 256;
-    for (int s = 0; s < c.n_steps; ++s) {
+    const long long rstride = (long long)a.H * D;
+    for (int s = 0; s < n_steps; ++s) {
         const uint32_t ts = ts_base + s;
-        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ]), ts & 1, abort, kTimeoutNs);
-        if (!named_and(2, 128, got)) return false;
-        tc::tc_fence_after();
         int h, p0, nrows;
-        step_rows(c, a, s, &h, &p0, &nrows);
-        uint32_t qv[2][32];
-        tc::tmem_ld32(tmem + lb + TDQ, qv[0]);
-        tc::tmem_ld32(tmem + lb + TDQ + 32, qv[1]);
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
+        long long qrow;
+        {   // before the wait: the decode reads the tile table from global memory
+            const ItemCtx c = decode(a, item);
+            step_rows(c, a, s, &h, &p0, &nrows);
+            qrow = q_row_of(a.lay, c.kt, p0);
+        }
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_DQ]), ts & 1, abort, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        tc::tc_fence_after();
+        if constexpr (D == 128) {
+            uint32_t v[4][32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            // staging buffer `half` was last read by the reduce issued one step ago
-            if (leader) bulk_wait_read1();
-            named_sync(2, 128);
-            float* stg = reinterpret_cast<float*>(smem + SM_STG + half * kStg) + dl;
+            for (int q = 0; q < 4; ++q) tc::tmem_ld32(tmem + lb + TRP + 32 * q, v[q]);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));  // RP may take dP^T(s+1)
+            // Stage the step's dq as fp32 [64 rows][128 d] in two buffers that
+            // are idle now (the dS^T buffer, read by dQ^T(s), and the dO(s)
+            // stage, read by dP^T(s) and dV(s)), and add each into the fp32
+            // accumulator with one TMA reduce-add. The dS^T buffer goes first
+            // and is released as soon as its reduce has read it, since the
+            // next step's dS^T waits for it. A warp writes 32 consecutive d
+            // of one row per store.
+            const uint32_t st = ts % kStages;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stg[e * D] = __uint_as_float(qv[half][e]);  // scaled in the convert kernel
-            tc::fence_proxy_async_smem();
-            named_sync(2, 128);
-            if (leader) {
-                tma_reduce_add_3d(tdq, sbase + SM_STG + half * kStg, 0, h, q_row_of(a.lay, c.kt, p0) + kHalfRows * half);
-                bulk_commit();
-                if (half == 1) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t buf = half == 0 ? L::S : L::O + st * L::kQT;
+                float* stg = reinterpret_cast<float*>(smem + buf) + dl;
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) stg[(32 * q + e) * D] = __uint_as_float(v[2 * half + q][e]);
+                tc::fence_proxy_async_smem();
+                named_sync_dq();
+                if (dl == 0) {
+                    if (64 * half < nrows) tma_reduce_add_3d(tdq, sbase + buf, 0, h, (int)(qrow + 64 * half));
+                    bulk_commit();
+                }
+            }
+            if (dl == 0) {
+                bulk_wait_read1();  // the dS^T buffer has been read
+                tc::mbar_arrive(tc::smem_addr(&bar[B_SF]));       // dS^T of the next step may be stored
+                bulk_wait_read0();  // the dO(s) stage has been read
+                tc::mbar_arrive(tc::smem_addr(&bar[B_OE + st]));  // dO of step s + 2 may be loaded
+            }
+        } else {
+            uint32_t v[2][32];
+            tc::tmem_ld32(tmem + lb + T::DQ, v[0]);
+            tc::tmem_ld32(tmem + lb + T::DQ + 32, v[1]);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_DQF]));  // dQ(s+1) may go
+            if (dl < nrows) {
+                float* dst = a.dqacc + (qrow + dl) * rstride + (long long)h * D;
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        red_add_v4f32(dst + 32 * q + e, __uint_as_float(v[q][e]), __uint_as_float(v[q][e + 1]),
+                                      __uint_as_float(v[q][e + 2]), __uint_as_float(v[q][e + 3]));
             }
         }
     }
-    // dK and dV: the last dQ^T commit covered every MMA of the item. Keys that
+    // dK and dV: the last dq commit covered every MMA of the item. Keys that
     // no query row of the call sees (clean keys after a block group's last
     // block) get zeros; their TMEM columns were never written for this item.
+    const ItemCtx c = decode(a, item);
     const int kk = dl;
     const bool key_ok = kk < c.kv_rows;
     const bool seen = c.n_steps > 0;
@@ -447,7 +570,7 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
     const long long rowoff = ((long long)slot * a.Lk + c.k0 + kk) * ((long long)a.Hk * D) + (long long)c.kvh * D;
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
-        const uint32_t src = which == 0 ? TDK : TDV;
+        const uint32_t src = which == 0 ? T::DK : T::DV;
         __nv_bfloat16* dst = (which == 0 ? a.dk : a.dv) + rowoff;
         const float mul = which == 0 ? a.scale : 1.f;
 #pragma unroll
@@ -475,39 +598,48 @@ __device__ __forceinline__ bool dq_item(const ItemCtx& c, const BwdArgs& a, uint
 }
 
 // ------------------------------------------------------------------ kernel
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = Smem<D>;
+    // everything lives in dynamic shared memory, whose base the 128-byte
+    // swizzled operand tiles need 1024-byte aligned
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = tc::smem_addr(smem);
-    __shared__ __align__(8) uint64_t bar[B_COUNT];
-    __shared__ __align__(16) StepInfo info[kStages];
-    __shared__ uint32_t s_tmem;
-    __shared__ int s_item;
-    __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (sbase & 1023u) {  // uniform over the CTA: nothing has been set up yet
+        if (tid == 0) set_error(a.hdr, DEV_CHECK, -3);
+        return;
+    }
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR);
+    StepInfo* info = reinterpret_cast<StepInfo*>(smem + L::INFO);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
+    int* s_item = reinterpret_cast<int*>(smem + L::MISC + 4);
+    int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 8);
 
     if (tid == 0) {
-        s_abort = 0;
+        *s_abort = 0;
         tc::mbar_init(tc::smem_addr(&bar[B_KV]), 1);
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(tc::smem_addr(&bar[B_QDF + s]), 32);  // the loader's 32 lanes, after their stores
-            tc::mbar_init(tc::smem_addr(&bar[B_QDE + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_QF + s]), 32);  // the loader's 32 lanes, after their stores
+            tc::mbar_init(tc::smem_addr(&bar[B_QE + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_OF + s]), 1);  // the loader's lane 0 (+ the dO bytes)
+            tc::mbar_init(tc::smem_addr(&bar[B_OE + s]), 1);  // the dq leader, after its reduce read the stage
         }
         tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_DP]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_SM]), 256);
-        tc::mbar_init(tc::smem_addr(&bar[B_SS]), 256);
-        tc::mbar_init(tc::smem_addr(&bar[B_SS + 1]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_P]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_DS]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_DSS]), 256);
         tc::mbar_init(tc::smem_addr(&bar[B_DQ]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_LD]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 4);  // lane 0 of each dq warp
+        tc::mbar_init(tc::smem_addr(&bar[B_SF]), 1);   // the dq leader
         tc::fence_barrier_init();
     }
     if (warp == 13) {
-        tc::tmem_alloc(tc::smem_addr(&s_tmem), kTmemCols);
+        tc::tmem_alloc(tc::smem_addr(s_tmem), kTmemCols);
         tc::tmem_relinquish();
     }
     if (warp == 12 && lane == 0) {
@@ -520,37 +652,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = s_tmem;
-    volatile int* abort = &s_abort;
+    const uint32_t tmem = *s_tmem;
+    volatile int* abort = s_abort;
     const int n_items = a.hdr->n_tiles * a.Hk;
+    // Every role runs its own copy of the item loop (so that setmaxnreg can
+    // give each role its register count); the loops meet at named barrier 1,
+    // all 512 threads, twice per item.
+    auto next_item = [&]() -> int {
+        named_sync_all();
+        if (tid == 0) *s_item = *abort ? n_items : atomicAdd(&a.hdr->counter, 1);
+        named_sync_all();
+        return *s_item;
+    };
     uint32_t ts_base = 0, item_count = 0;
-    for (;;) {
-        __syncthreads();
-        if (tid == 0) s_item = *abort ? n_items : atomicAdd(&a.hdr->counter, 1);
-        __syncthreads();
-        const int item = s_item;
-        if (item >= n_items) break;
-        const ItemCtx c = decode(a, item);
-        if (warp == 12) {
-            load_item(c, a, sbase, bar, info, &tm_k, &tm_v, &tm_q, &tm_do, ts_base, abort);
-        } else if (warp == 13) {
-            if (lane == 0) issue_item(c, sbase, bar, tmem, ts_base, item_count, abort);
-        } else if (warp < 8) {
-            pds_item(c, a, smem, bar, info, tmem, ts_base, abort);
-        } else {
-            dq_item(c, a, sbase, smem, bar, tmem, &tm_dq, ts_base, abort);
+    if (warp >= 12) {
+        tc::regs_dec<kRegsIo>();
+        for (int item; (item = next_item()) < n_items;) {
+            const ItemCtx c = decode(a, item);
+            if (warp == 12)
+                load_item<D>(c, a, sbase, bar, info, &tm_k, &tm_v, &tm_q, &tm_do, ts_base, abort);
+            else if (warp == 13 && lane == 0)
+                issue_item<D>(c, sbase, bar, tmem, ts_base, item_count, abort);
+            // warps 14-15 only complete the warpgroup
+            ts_base += c.n_steps;
+            ++item_count;
         }
-        ts_base += c.n_steps;
-        ++item_count;
+    } else if (warp >= 8) {
+        tc::regs_inc<kRegsDq>();
+        for (int item; (item = next_item()) < n_items;) {
+            const int n_steps = decode(a, item).n_steps;
+            dq_item<D>(item, n_steps, a, smem, sbase, bar, tmem, &tm_dq, ts_base, abort);
+            ts_base += n_steps;
+        }
+    } else {
+        tc::regs_inc<kRegsPds>();
+        for (int item; (item = next_item()) < n_items;) {
+            const ItemCtx c = decode(a, item);
+            pds_item<D>(c, a, smem, bar, info, tmem, ts_base, abort);
+            ts_base += c.n_steps;
+        }
     }
-    if (tid == 256) bulk_wait0();  // every dq reduce has landed
+    if (D == 128 && tid == 256) bulk_wait0();  // every dq reduce-add has landed
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 13) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
-    if (tid == 0 && s_abort) set_error(a.hdr, DEV_TIMEOUT, blockIdx.x);
+    if (tid == 0 && *s_abort) set_error(a.hdr, DEV_TIMEOUT, blockIdx.x);
 }
 
 // ------------------------------------------------------------- host side
@@ -572,35 +721,52 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows, heads, D] tensor as a 3-D map (D, heads, rows) with (box_d, 1, box_rows) boxes.
-bool make_map(CUtensorMap* m, const void* base, bool f32, int heads, long long rows, int box_d, int box_rows,
-              CUtensorMapSwizzle sw) {
+// bf16 [rows, heads, d] tensor as a 3-D map (d, heads, rows) with 64 x 1 x
+// box_rows boxes, 128-byte swizzled.
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const int esz = f32 ? 4 : 2;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)heads * D * esz};
-    cuuint32_t box[3] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The fp32 dq accumulator [rows, heads, d] as a 3-D map (d, heads, rows) with
+// d x 1 x 64 boxes, unswizzled: the target of the staged reduce-adds.
+bool make_acc_map(CUtensorMap* m, float* base, int d, int heads, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_t(const BwdArgs& a, int num_sms, cudaStream_t st) {
+    CUtensorMap mk, mv, mq, mdo, mdq;
+    if (!make_map(&mk, a.k, D, a.Hk, a.Lk, BN) || !make_map(&mv, a.v, D, a.Hk, a.Lk, BN) ||
+        !make_map(&mq, a.q, D, a.H, a.Lq, BQ) || !make_map(&mdo, a.dO, D, a.H, a.Lq, BQ) ||
+        !make_acc_map(&mdq, a.dqacc, D, a.H, a.Lq))
+        return cudaErrorInvalidValue;
+    constexpr int smem = Smem<D>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    bwd_tc_kernel<D><<<num_sms, kThreads, smem, st>>>(mk, mv, mq, mdo, mdq, a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st) {
-    CUtensorMap mk, mv, mq, mdo, mdq;
-    if (!make_map(&mk, a.k, false, a.Hk, a.Lk, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, a.v, false, a.Hk, a.Lk, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mq, a.q, false, a.H, a.Lq, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdo, a.dO, false, a.H, a.Lq, 64, BQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdq, a.dqacc, true, a.H, a.Lq, D, kHalfRows, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    bwd_tc_kernel<<<num_sms, kThreads, kSmemBytes, st>>>(mk, mv, mq, mdo, mdq, a);
-    return cudaGetLastError();
+    return a.D == 128 ? launch_t<128>(a, num_sms, st) : launch_t<64>(a, num_sms, st);
 }
 
 }  // namespace bdlm

@@ -81,6 +81,7 @@ void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, 
 cudaError_t launch_fwd_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_bwd_tc64_main(const BwdArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st, int* launches);
 
 // Device address of the no-allocation forward's fixed scratch on the current
