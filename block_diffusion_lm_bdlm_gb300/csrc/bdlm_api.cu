@@ -36,8 +36,8 @@ int num_sms() {
 }
 
 long long max_tiles_for(long long L, int n_docs) {
-    // the smallest tile height any kernel enumerates is 64 rows; every document
-    // half can add one ragged tile
+    // the kernels enumerate tiles of 128 rows (keys); this bound allows one
+    // per 64, with room to spare, plus one ragged tile per document half
     return L / 64 + 2LL * (n_docs > 0 ? n_docs : 1) + 4;
 }
 
@@ -88,8 +88,7 @@ constexpr int kMaxTasks = 65536;
 constexpr int kMaxSlots = 1024;
 
 // Tiles of one task: forward - its query positions in 128-row tiles;
-// backward - its key positions in 64-key tiles (the smaller backward tile);
-// each in two runs split at n.
+// backward - its key positions in 128-key tiles; each in two runs split at n.
 long long task_tiles(const bdlm_task& t, bool bwd) {
     const long long rows = bwd ? kBwdKeyTile : kFwdTileRows;
     auto run = [rows](long long lo, long long hi) { return hi > lo ? (hi - lo + rows - 1) / rows : 0; };
@@ -390,7 +389,7 @@ int bdlm_attn_bwd_tasks(const void* q, const void* k, const void* v, const void*
     lay.L = L;
     lay.tasks = ws.tasks;
     lay.n_tasks = n_tasks;
-    launch_enumerate(lay, head_dim == 128 ? kBwdTcKeyTile : kBwdKeyTile, kBwdQTile, 1, ws, s);
+    launch_enumerate(lay, kBwdKeyTile, kBwdQTile, 1, ws, s);
     if (cudaGetLastError() != cudaSuccess) return BDLM_ERR_CUDA;
     ++launches;
 
@@ -444,7 +443,7 @@ int bdlm_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
 
     WsCarve ws = carve(workspace, L, docs, heads, head_dim, true);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    launch_enumerate(lay, head_dim == 128 ? kBwdTcKeyTile : kBwdKeyTile, kBwdQTile, 1, ws, s);
+    launch_enumerate(lay, kBwdKeyTile, kBwdQTile, 1, ws, s);
     if (cudaGetLastError() != cudaSuccess) return BDLM_ERR_CUDA;
     int launches = 1;
 

@@ -69,9 +69,8 @@ struct MergeArgs {
 // Tile heights used by the kernels (the prologue enumerates in these units).
 constexpr int kFwdTileRows = 128;  // tensor-core forward: 128-row query tiles
 constexpr int kFwdKeyTile = 128;   // and 128-key steps
-constexpr int kBwdKeyTile = 64;     // warp-level backward (head_dim 64)
-constexpr int kBwdTcKeyTile = 128;  // tensor-core backward (head_dim 128)
-constexpr int kBwdQTile = 64;
+constexpr int kBwdKeyTile = 128;  // backward: 128-key items
+constexpr int kBwdQTile = 128;    // and 128-row query steps
 
 // Task records per upload launch (kernel parameters stay under 32 KB).
 constexpr int kTaskUploadChunk = 960;
@@ -81,7 +80,6 @@ void launch_enumerate(const Layout& lay, int tile_rows, int key_tile, int kind, 
 cudaError_t launch_fwd_tc(const FwdArgs& a, const TileRange* ranges, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t st, int* launches);
 cudaError_t launch_bwd_tc_main(const BwdArgs& a, int num_sms, cudaStream_t st);
-cudaError_t launch_bwd_tc64_main(const BwdArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st, int* launches);
 
 // Device address of the no-allocation forward's fixed scratch on the current
