@@ -9,6 +9,12 @@ Metric: valid-pair TFLOP/s, FLOPs = 4*d*H*P (forward) + 10*d*H*P (backward),
 P = n(n + B) valid (query, key) pairs per head.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME]
+
+The other workloads of synth run laid out as they are stated: the 8K + 8K
+and packed-document workloads as one forward and one backward, the 256K +
+256K workload as its clean rows plus its 16 early/late block groups (see
+Step).
 
 Prints one JSON line (rank 0). With --gpus N > 1 (torchrun) every rank runs
 an independent replica of the step on its own GPU; the timing is the max over
@@ -243,23 +249,36 @@ def run_reference(args, rank, world):
 # the CUDA arm
 # ----------------------------------------------------------------------------
 class Step:
-    """One pass of the hot path over one batch: for one sequence, the partial
-    forwards against the clean shards and the local corrupted keys, their
-    merge and the backward; for packed documents (no shards), the forward and
-    backward over cu_seqlens."""
+    """One pass of the hot path over one batch, laid out as the workload
+    states it:
+      shards  the partial forwards against the contiguous clean-K/V shards
+              and the local corrupted keys, their LSE merge, the backward;
+      full    one forward and one backward over the sequence, or over the
+              packed documents (cu_seqlens);
+      groups  block parallelism: the clean rows' forward against the clean
+              keys, then every early/late block group's forward (its
+              corrupted rows against all clean keys and its own corrupted
+              keys), then the same backwards. The groups' shares of the clean
+              keys' dk, dv stay per group, as on the ranks that own them (their
+              sum is a multi-GPU reduction, out of scope on one GPU); each
+              group's inputs are laid out once, before any timing, as a
+              rank would hold them."""
 
     def __init__(self, bd, w, x, dev):
         self.bd, self.w, self.x = bd, w, x
         H, d = w.heads, w.head_dim
         self.cu = None
+        self.mode = "full" if w.docs else ("shards" if w.shards else ("groups" if w.groups else "full"))
+        self.windows = []
         if w.docs:
             self.cu = torch.tensor(x.cu_seqlens, dtype=torch.int32, device=dev)
             L, n_docs = x.cu_seqlens[-1], w.docs
-            self.windows = []
         else:
             n = w.n
             L, n_docs = 2 * n, 1
-            self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+            if self.mode == "shards":
+                self.windows = synth.shard_bounds(n, w.shards) + [(n, 2 * n)]
+        self.groups = self._layout_groups(dev) if self.mode == "groups" else []
         # the partials as one [P, L, H, d] buffer (and [P, H, L] lse): the
         # window calls write its slices, a task list writes its slots
         P = len(self.windows)
@@ -279,6 +298,58 @@ class Step:
         self.ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d, n_docs), dtype=torch.uint8, device=dev)
         self.launches = 0
 
+    def _layout_groups(self, dev):
+        """Per group: its block list and its gathered q, k, v, dO (q, dO: the
+        corrupted rows of its blocks; k, v: the n clean rows, then those rows),
+        with its outputs; plus the clean rows (views of the inputs)."""
+        w, x = self.w, self.x
+        n, B, H = w.n, w.block, w.heads
+        ar = torch.arange(B, device=dev)
+        clean = torch.arange(n, device=dev)
+        gs = []
+        for blocks in synth.early_late_groups((n + B - 1) // B, w.groups):
+            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
+            corr = (n + bl.long()[:, None] * B + ar[None]).reshape(-1)
+            kpos = torch.cat([clean, corr])
+            g = dict(bl=bl, q=x.q[corr].contiguous(), k=x.k[kpos].contiguous(), v=x.v[kpos].contiguous(),
+                     do=x.do[corr].contiguous())
+            g["o"] = torch.empty_like(g["q"])
+            g["lse"] = torch.empty((H, g["q"].shape[0]), dtype=torch.float32, device=dev)
+            g["dq"], g["dk"], g["dv"] = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+            gs.append(g)
+        c = dict(q=x.q[:n], k=x.k[:n], v=x.v[:n], do=x.do[:n], o=torch.empty_like(x.q[:n]),
+                 lse=torch.empty((H, n), dtype=torch.float32, device=dev), dq=torch.empty_like(x.q[:n]),
+                 dk=torch.empty_like(x.k[:n]), dv=torch.empty_like(x.v[:n]))
+        self.clean = c
+        return gs
+
+    def _groups_fwd(self):
+        bd, w = self.bd, self.w
+        n, B, c = w.n, w.block, self.clean
+        launches = 0
+        bd.bdlm_attn_fwd(c["q"], c["k"], c["v"], B, L=2 * n, part=bd.Partial.window(0, n, q_lo=0, q_hi=n),
+                         out=c["o"], lse=c["lse"], workspace=self.ws_f)
+        launches += bd.bdlm_last_launch_count()
+        for g in self.groups:
+            bd.bdlm_attn_fwd(g["q"], g["k"], g["v"], B, L=2 * n, part=bd.Partial.group(g["bl"]), out=g["o"],
+                             lse=g["lse"], workspace=self.ws_f)
+            launches += bd.bdlm_last_launch_count()
+        return launches
+
+    def _groups_bwd(self):
+        bd, w = self.bd, self.w
+        n, B, c = w.n, w.block, self.clean
+        launches = 0
+        bd.bdlm_attn_bwd(c["q"], c["k"], c["v"], c["o"], c["lse"], c["do"], B, L=2 * n,
+                         part=bd.Partial.window(0, n, q_lo=0, q_hi=n), dq=c["dq"], dk=c["dk"], dv=c["dv"],
+                         workspace=self.ws_b)
+        launches += bd.bdlm_last_launch_count()
+        for g in self.groups:
+            bd.bdlm_attn_bwd(g["q"], g["k"], g["v"], g["o"], g["lse"], g["do"], B, L=2 * n,
+                             part=bd.Partial.group(g["bl"]), dq=g["dq"], dk=g["dk"], dv=g["dv"], workspace=self.ws_b)
+            launches += bd.bdlm_last_launch_count()
+        return launches
+
     def run(self, ev=None, after_fwd=None):
         """One step; `after_fwd` (if given) is called between the forward
         (with its merge) and the backward."""
@@ -290,9 +361,11 @@ class Step:
             bd.bdlm_attn_fwd(x.q, x.k[lo:hi], x.v[lo:hi], w.block, part=bd.Partial.window(lo, hi), out=po, lse=pl,
                              workspace=self.ws_f)
             launches += bd.bdlm_last_launch_count()
-        if self.cu is not None:
+        if self.mode == "full":
             bd.bdlm_attn_fwd(x.q, x.k, x.v, w.block, cu_seqlens=self.cu, out=self.o, lse=self.lse, workspace=self.ws_f)
             launches += bd.bdlm_last_launch_count()
+        elif self.mode == "groups":
+            launches += self._groups_fwd()
         if ev:
             ev[1].record()
         if self.windows:
@@ -302,9 +375,12 @@ class Step:
             ev[2].record()
         if after_fwd:
             after_fwd()
-        bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, cu_seqlens=self.cu, dq=self.dq, dk=self.dk,
-                         dv=self.dv, workspace=self.ws_b)
-        launches += bd.bdlm_last_launch_count()
+        if self.mode == "groups":
+            launches += self._groups_bwd()
+        else:
+            bd.bdlm_attn_bwd(x.q, x.k, x.v, self.o, self.lse, x.do, w.block, cu_seqlens=self.cu, dq=self.dq,
+                             dk=self.dk, dv=self.dv, workspace=self.ws_b)
+            launches += bd.bdlm_last_launch_count()
         if ev:
             ev[3].record()
         self.launches += launches
@@ -346,66 +422,6 @@ class Step:
             out.append(statistics.median(times))
         del ws_b
         return out[0], out[1]
-
-    def time_groups(self, reps=2):
-        """Block parallelism on one GPU: the forward and the backward of each
-        early/late block group of the workload (the corrupted rows of its
-        blocks against all clean keys and their own corrupted keys), the
-        groups run one after another; not part of the timed step. Inputs are
-        gathered before timing. Returns (fwd ms, bwd ms, fwd FLOP, bwd FLOP)
-        medians over `reps` runs after one warm-up, or None without groups."""
-        bd, w, x = self.bd, self.w, self.x
-        if not w.groups or w.docs:
-            return None
-        n, B = w.n, w.block
-        dev = x.q.device
-        groups = synth.early_late_groups(n // B, w.groups)
-        ar = torch.arange(B, device=dev)
-        clean = torch.arange(n, device=dev)
-        L, H, d = x.q.shape
-        ws_f = torch.empty(bd.bdlm_attn_fwd_workspace_bytes(L, H, d), dtype=torch.uint8, device=dev)
-        ws_b = torch.empty(bd.bdlm_attn_bwd_workspace_bytes(L, H, d), dtype=torch.uint8, device=dev)
-        gs = []
-        pairs = 0
-        for blocks in groups:
-            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
-            corr = (n + bl.long()[:, None] * B + ar[None]).reshape(-1)
-            kpos = torch.cat([clean, corr])
-            g = dict(bl=bl, q=x.q[corr].contiguous(), k=x.k[kpos].contiguous(), v=x.v[kpos].contiguous(),
-                     do=x.do[corr].contiguous())
-            g["o"] = torch.empty_like(g["q"])
-            g["lse"] = torch.empty((H, g["q"].shape[0]), dtype=torch.float32, device=dev)
-            g["dq"], g["dk"], g["dv"] = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
-            gs.append(g)
-            # a corrupted row of block b sees b*B clean keys and its B own keys
-            pairs += sum(B * (b * B + B) for b in blocks)
-        f_fwd, f_bwd = 4 * d * H * pairs, 10 * d * H * pairs
-
-        def fwd():
-            for g in gs:
-                bd.bdlm_attn_fwd(g["q"], g["k"], g["v"], B, L=2 * n, part=bd.Partial.group(g["bl"]), out=g["o"],
-                                 lse=g["lse"], workspace=ws_f)
-
-        def bwd():
-            for g in gs:
-                bd.bdlm_attn_bwd(g["q"], g["k"], g["v"], g["o"], g["lse"], g["do"], B, L=2 * n,
-                                 part=bd.Partial.group(g["bl"]), dq=g["dq"], dk=g["dk"], dv=g["dv"], workspace=ws_b)
-
-        out = []
-        for f in (fwd, bwd):
-            f()
-            times = []
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                f()
-                e1.record()
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1))
-            out.append(statistics.median(times))
-        del gs, ws_f, ws_b
-        torch.cuda.empty_cache()
-        return out[0], out[1], f_fwd, f_bwd
 
     def time_graph(self, reps=5):
         """The step captured once in a CUDA graph and replayed (every library
@@ -504,8 +520,6 @@ def run_cuda(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.BY_NAME[args.workload]
-    if not w.shards and not w.docs:
-        w = synth.Workload(**{**w.__dict__, "shards": 8})
     log(f"[rank {rank}] generating inputs for {w.name}")
     x = synth.make_inputs(w, device="cuda")
     step = Step(bd, w, x, dev)
@@ -547,14 +561,13 @@ def run_cuda(args, rank, world, local):
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     run_ms = step.time_running_merge()
     task_ms, task_bwd_ms = step.time_task_list()
-    groups = step.time_groups()
     graph_ms = step.time_graph()
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and step.mode != "groups":
         e2e = end_to_end(step, x, flops, args, world, dev)
     _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms,
-            task_bwd_ms, groups, graph_ms)
+            task_bwd_ms, graph_ms)
 
 
 def end_to_end(step, x, flops, args, world, dev):
@@ -663,7 +676,7 @@ def l2_note(x):
 
 def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per_step, value, fwd_ms, mrg_ms,
             bwd_ms, achieved, peak, peak_kind, peaks, e2e, launches, clocks, run_ms, step_ms, task_ms, task_bwd_ms,
-            groups=None, graph_ms=None):
+            graph_ms=None):
     traffic = None
     if TRAFFIC["sha1"] and source_sha(TRAFFIC["kernel_sources"]) == TRAFFIC["sha1"]:
         traffic = TRAFFIC["bytes_per_launch"]
@@ -674,7 +687,8 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "n_clean": w.n, "n_corrupted": w.n, "docs": w.docs or 1,
                    "rows": x.q.shape[0], "block": w.block, "heads": w.heads,
-                   "kv_heads": w.kv_heads, "head_dim": w.head_dim, "clean_shards": w.shards,
+                   "kv_heads": w.kv_heads, "head_dim": w.head_dim, "layout": step.mode, "clean_shards": w.shards,
+                   "block_groups": w.groups,
                    "l2": l2_note(x), "parallelism": f"replicas{world}"},
         "roofline": {"kernel": "bdlm_attn_bwd (key-major main kernel + preprocess + dq convert)",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -695,11 +709,6 @@ def _report(args, rank, world, w, step, x, flops, f_fwd, f_bwd, total_ms, ms_per
             "fwd_task_list_tflops": f_fwd / (task_ms / 1e3) / 1e12 if task_ms else None,
             "bwd_task_list_ms": task_bwd_ms,
             "bwd_task_list_tflops": f_bwd / (task_bwd_ms / 1e3) / 1e12 if task_bwd_ms else None,
-            # block groups (block parallelism): every group's forward, then every group's backward
-            "groups_fwd_ms": groups[0] if groups else None,
-            "groups_fwd_tflops": groups[2] / (groups[0] / 1e3) / 1e12 if groups else None,
-            "groups_bwd_ms": groups[1] if groups else None,
-            "groups_bwd_tflops": groups[3] / (groups[1] / 1e3) / 1e12 if groups else None,
             "step_ms_min": step_ms[0], "step_ms_median": statistics.median(step_ms), "step_ms_max": step_ms[-1],
             # the same step replayed from a CUDA graph (outside the timed steps)
             "step_graph_ms": graph_ms,

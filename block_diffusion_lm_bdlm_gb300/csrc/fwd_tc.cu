@@ -20,9 +20,10 @@
 // TMEM (512 columns): S0 | S1 | O0 | O1; P_i (bf16) overwrites the first 64
 // columns of S_i after the softmax group has read S_i into registers.
 // Per key tile j (128 keys):  S_i = Q_i K_j^T  ->  softmax_i  ->  O_i += P_i V_j.
-// The next S_i is issued only after the previous O_i += P_i V MMA has
-// completed (it reads P_i, which S_i overwrites); with two heads in flight the
-// tensor pipe stays fed during that wait.
+// The next S_i is issued right behind O_i += P_i V_j: the tensor pipe runs a
+// CTA's MMAs in issue order, so the PV MMA reads P_i before S_i overwrites
+// it, and the softmax, which waits for S_i's commit, sees O_i complete (an
+// MMA's commit covers every MMA issued before it) before it rescales O_i.
 // Online softmax in fp32 registers, base 2, with a lazily moved offset: the
 // running row offset changes only when the row max exceeds it by more than
 // 2^8, and only then is the O row in TMEM rescaled.
@@ -126,28 +127,27 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
     // MN-major (V); tiles, K slices and stages are constant offsets
     const uint64_t km = tc::sdesc_sw128(sbase, 16, 1024);
     const uint64_t mn = tc::sdesc_sw128(sbase, S::kChunk, 1024);
-    for (int j = 0; j < c.nk; ++j) {
-        const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
+    // S_i = Q_i K_j^T into head i's S columns
+    auto issue_s = [&](int i, uint32_t stage) {
+        const uint64_t dK = tc::sdesc_add(km, S::kK + stage * S::kTile);
+        const uint64_t dQ = tc::sdesc_add(km, i == 0 ? S::kQ0 : S::kQ1);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * S::kChunk + (k & 3) * 32;
+            tc::mma_ss(tmem + 128 * i, tc::sdesc_add(dQ, off), tc::sdesc_add(dK, off), idesc_s, k > 0);
+        }
+        tc::mma_commit(tc::smem_addr(&bar[B_S + i]));
+    };
+    if (c.nk == 0) return;
+    {
+        const uint32_t t = t_base, s = t & 1, ph = (t >> 1) & 1;
         if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + s]), ph, abort, kTimeoutNs)) return;
         tc::tc_fence_after();
-        const uint64_t dK = tc::sdesc_add(km, S::kK + s * S::kTile);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if (i >= nh) break;
-            const uint32_t ti = i == 0 ? t : t_base1 + j;
-            const uint32_t tS = tmem + 128 * i;
-            const uint64_t dQ = tc::sdesc_add(km, i == 0 ? S::kQ0 : S::kQ1);
-            if (j > 0) {  // O_i += P_i V of the previous tile has read P_i
-                if (!tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), (ti - 1) & 1, abort, kTimeoutNs)) return;
-                tc::tc_fence_after();
-            }
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * S::kChunk + (k & 3) * 32;
-                tc::mma_ss(tS, tc::sdesc_add(dQ, off), tc::sdesc_add(dK, off), idesc_s, k > 0);
-            }
-            tc::mma_commit(tc::smem_addr(&bar[B_S + i]));
-        }
+        for (int i = 0; i < nh; ++i) issue_s(i, s);
+    }
+    for (int j = 0; j < c.nk; ++j) {
+        const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
+        const uint32_t tn = t + 1, sn = tn & 1, phn = (tn >> 1) & 1;
         if (!tc::mbar_wait(tc::smem_addr(&bar[B_VFULL + s]), ph, abort, kTimeoutNs)) return;
         const uint64_t dV = tc::sdesc_add(mn, S::kV + s * S::kTile);
 #pragma unroll
@@ -168,8 +168,18 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
             for (int k = BN / 32; k < BN / 16; ++k)
                 tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, 1u);
             tc::mma_commit(tc::smem_addr(&bar[B_O + i]));
+            if (i == nh - 1) tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));  // K_j, V_j read
+            // S_i of the next key tile right behind PV_i: the tensor pipe runs
+            // this CTA's MMAs in issue order, so it reads P_i before S_i
+            // overwrites it, and its commit covers PV_i
+            if (j + 1 < c.nk) {
+                if (i == 0) {
+                    if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + sn]), phn, abort, kTimeoutNs)) return;
+                    tc::tc_fence_after();
+                }
+                issue_s(i, sn);
+            }
         }
-        tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));
     }
 }
 
