@@ -82,12 +82,16 @@ def merge_bytes(w, n_parts):
 
 
 def mufu_exp_peak(clocks):
-    """Exponentials per second the special-function units can issue: 16 ex2
-    per clock per SM (4 per SM sub-partition), times the SM count, at the
-    median SM clock sampled under load (the maximum clock when no sample)."""
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    """Exponentials per second the special-function units can issue, times
+    the SM count, at the median SM clock sampled under load (the maximum
+    clock when no sample): 32 ex2 per clock per SM on compute capability 10.3
+    (GB300 doubles the exponential rate of the sm_100 parts, 16 per clock per
+    SM; a timing probe of ex2.approx.ftz.f32 with one packed FMA per pair, two
+    warps per SM sub-partition on all SMs, measured about 29 per clock)."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    per_clk = 32.0 if (props.major, props.minor) == (10, 3) else 16.0
     mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070
-    return 16.0 * sms * float(mhz) * 1e6
+    return per_clk * props.multi_processor_count * float(mhz) * 1e6
 
 
 def load_peaks():

@@ -24,6 +24,13 @@
 // CTA's MMAs in issue order, so the PV MMA reads P_i before S_i overwrites
 // it, and the softmax, which waits for S_i's commit, sees O_i complete (an
 // MMA's commit covers every MMA issued before it) before it rescales O_i.
+// The tensor pipe holds little more than the MMA it is running, so each wait,
+// fence or commit of the issuing thread leaves it idle for about as long as
+// that step takes. The issuer therefore waits once per key tile for K_j and
+// V_j together (one barrier), once per head for the whole of P_i, and
+// commits O_i only after the item's last key tile.
+// A key tile with masked entries is masked in TMEM (-inf written over the
+// entries) before the softmax reads it, so unmasked tiles run no mask code.
 // Online softmax in fp32 registers, base 2, with a lazily moved offset: the
 // running row offset changes only when the row max exceeds it by more than
 // 2^8, and only then is the O row in TMEM rescaled.
@@ -58,7 +65,7 @@ struct Lay {
 };
 
 // barrier slots
-enum : int { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_S = 7, B_P = 9, B_O = 11, B_PH = 13, B_COUNT = 15 };
+enum : int { B_Q = 0, B_KVFULL = 1, B_KVEMPTY = 3, B_S = 5, B_P = 7, B_O = 9, B_COUNT = 11 };
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -102,13 +109,13 @@ __device__ __forceinline__ void produce(const ItemCtx& c, uint32_t sbase, const 
         const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
         if (!tc::mbar_wait(tc::smem_addr(&bar[B_KVEMPTY + s]), ph ^ 1, abort, kTimeoutNs)) return;
         const int k0 = key_start(c.R, c.n1, j);
-        const uint32_t bk = tc::smem_addr(&bar[B_KFULL + s]), bv = tc::smem_addr(&bar[B_VFULL + s]);
-        tc::mbar_arrive_expect_tx(bk, S::kTile);
+        // K_j and V_j complete one barrier: the MMA issuer waits once per key tile
+        const uint32_t bkv = tc::smem_addr(&bar[B_KVFULL + s]);
+        tc::mbar_arrive_expect_tx(bkv, 2 * S::kTile);
         for (int ch = 0; ch < NC; ++ch)
-            tc::tma_load_3d(sbase + S::kK + s * S::kTile + ch * S::kChunk, tk, bk, 64 * ch, c.kvh, k0);
-        tc::mbar_arrive_expect_tx(bv, S::kTile);
+            tc::tma_load_3d(sbase + S::kK + s * S::kTile + ch * S::kChunk, tk, bkv, 64 * ch, c.kvh, k0);
         for (int ch = 0; ch < NC; ++ch)
-            tc::tma_load_3d(sbase + S::kV + s * S::kTile + ch * S::kChunk, tv, bv, 64 * ch, c.kvh, k0);
+            tc::tma_load_3d(sbase + S::kV + s * S::kTile + ch * S::kChunk, tv, bkv, 64 * ch, c.kvh, k0);
     }
 }
 
@@ -141,40 +148,34 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
     if (c.nk == 0) return;
     {
         const uint32_t t = t_base, s = t & 1, ph = (t >> 1) & 1;
-        if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + s]), ph, abort, kTimeoutNs)) return;
+        if (!tc::mbar_wait(tc::smem_addr(&bar[B_KVFULL + s]), ph, abort, kTimeoutNs)) return;
         tc::tc_fence_after();
         for (int i = 0; i < nh; ++i) issue_s(i, s);
     }
     for (int j = 0; j < c.nk; ++j) {
         const uint32_t t = t_base + j, s = t & 1, ph = (t >> 1) & 1;
         const uint32_t tn = t + 1, sn = tn & 1, phn = (tn >> 1) & 1;
-        if (!tc::mbar_wait(tc::smem_addr(&bar[B_VFULL + s]), ph, abort, kTimeoutNs)) return;
         const uint64_t dV = tc::sdesc_add(mn, S::kV + s * S::kTile);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             if (i >= nh) break;
             const uint32_t ti = i == 0 ? t : t_base1 + j;
             const uint32_t tS = tmem + 128 * i, tO = tmem + 256 + D * i;
-            // P arrives in two halves (keys 0-63, then 64-127) so that the
-            // first half's PV overlaps the softmax of the second half
-            if (!tc::mbar_wait(tc::smem_addr(&bar[B_PH + i]), ti & 1, abort, kTimeoutNs)) return;
-            tc::tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < BN / 32; ++k)
-                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+            // one wait for the whole of P_i: every wait of this thread leaves
+            // the tensor pipe idle for as long as it takes
             if (!tc::mbar_wait(tc::smem_addr(&bar[B_P + i]), ti & 1, abort, kTimeoutNs)) return;
             tc::tc_fence_after();
 #pragma unroll
-            for (int k = BN / 32; k < BN / 16; ++k)
-                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, 1u);
-            tc::mma_commit(tc::smem_addr(&bar[B_O + i]));
+            for (int k = 0; k < BN / 16; ++k)
+                tc::mma_ts(tO, tS + 8 * k, tc::sdesc_add(dV, 2048 * k), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+            if (j + 1 == c.nk) tc::mma_commit(tc::smem_addr(&bar[B_O + i]));  // O_i complete
             if (i == nh - 1) tc::mma_commit(tc::smem_addr(&bar[B_KVEMPTY + s]));  // K_j, V_j read
             // S_i of the next key tile right behind PV_i: the tensor pipe runs
             // this CTA's MMAs in issue order, so it reads P_i before S_i
             // overwrites it, and its commit covers PV_i
             if (j + 1 < c.nk) {
                 if (i == 0) {
-                    if (!tc::mbar_wait(tc::smem_addr(&bar[B_KFULL + sn]), phn, abort, kTimeoutNs)) return;
+                    if (!tc::mbar_wait(tc::smem_addr(&bar[B_KVFULL + sn]), phn, abort, kTimeoutNs)) return;
                     tc::tc_fence_after();
                 }
                 issue_s(i, sn);
@@ -190,7 +191,7 @@ __device__ __forceinline__ void issue_mma(const ItemCtx& c, uint32_t sbase, cons
 // warp-collective, so every branch around them is warp-uniform.
 template <int D>
 __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a, const uint64_t* bar, uint32_t tmem,
-                                             int i, uint32_t tb, volatile int* abort,
+                                             int i, uint32_t tb, uint32_t o_count, volatile int* abort,
                                              const int* item_p) {
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16;
@@ -206,6 +207,24 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_S + i]), t & 1, abort, kTimeoutNs);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc::tc_fence_after();
+        const int k0 = key_start(c.R, c.n1, j);
+        const bool full = j < c.n1 && k0 >= c.R.full_lo && k0 + BN <= c.R.full_hi;  // warp-uniform
+        if (!full) {
+            // a tile with masked entries: write -inf over them in TMEM first,
+            // so that the path of unmasked tiles carries no mask code
+            const RelInterval ri = range_interval(sp, j < c.n1, k0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t m[32];
+                tc::tmem_ld32(tS + 32 * q, m);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (!rel_sees(ri, 32 * q + e)) m[e] = 0xff800000u;  // -inf
+                tc::tmem_st32(tS + 32 * q, m);
+            }
+            tc::tmem_st_wait();
+        }
         uint32_t r[4][32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) tc::tmem_ld32(tS + 32 * q, r[q]);
@@ -215,14 +234,6 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[32 * q + e] = __uint_as_float(r[q][e]);
-        const int k0 = key_start(c.R, c.n1, j);
-        const bool full = j < c.n1 && k0 >= c.R.full_lo && k0 + BN <= c.R.full_hi;
-        if (!full) {
-            const RelInterval ri = range_interval(sp, j < c.n1, k0);
-#pragma unroll
-            for (int e = 0; e < 128; ++e)
-                if (!rel_sees(ri, e)) x[e] = -INFINITY;
-        }
         // row max, four independent chains of three-input max
         float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
@@ -264,9 +275,6 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
             pa[e] = pack2(p.x, p.y);
         }
         tc::tmem_st32(tS, pa);
-        tc::tmem_st_wait();
-        tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_PH + i]));
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             const float2 y = tc::fma2(make_float2(x[64 + 2 * e], x[64 + 2 * e + 1]), sl2x2, nm2);
@@ -281,7 +289,7 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         tc::mbar_arrive(tc::smem_addr(&bar[B_P + i]));
     }
     if (ok && c.nk > 0) {
-        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), (tb + c.nk - 1) & 1, abort, kTimeoutNs);
+        const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), o_count & 1, abort, kTimeoutNs);
         ok = __all_sync(0xffffffffu, got);
         tc::tc_fence_after();
     }
@@ -403,12 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 0;
         tc::mbar_init(tc::smem_addr(&bar[B_Q]), 1);
         for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(tc::smem_addr(&bar[B_KFULL + s]), 1);
-            tc::mbar_init(tc::smem_addr(&bar[B_VFULL + s]), 1);
+            tc::mbar_init(tc::smem_addr(&bar[B_KVFULL + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_KVEMPTY + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_S + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_P + s]), 128);
-            tc::mbar_init(tc::smem_addr(&bar[B_PH + s]), 128);
             tc::mbar_init(tc::smem_addr(&bar[B_O + s]), 1);
         }
         tc::fence_barrier_init();
@@ -453,13 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         tc::regs_inc<kRegsSoftmax>();
         const int wg = warp >> 2;
+        uint32_t o_count = 0;  // items with key tiles that this head slot has finished
         for (;;) {
             named_sync();
             named_sync();
             const int item = s_item;
             if (item >= n_items) break;
             const ItemCtx c = decode(a, ranges, item, n_pairs, per_kv);
-            if (wg == 0 || c.two) softmax_rows<D>(c, a, bar, tmem, wg, wg == 0 ? t_base : t_base1, abort, &s_item);
+            if (wg == 0 || c.two) {
+                softmax_rows<D>(c, a, bar, tmem, wg, wg == 0 ? t_base : t_base1, o_count, abort, &s_item);
+                if (c.nk > 0) ++o_count;
+            }
             t_base += c.nk;
             if (c.two) t_base1 += c.nk;
         }
