@@ -446,7 +446,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         tc::tmem_st32(tS, pk);
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_P]));  // dV(s) and then S^T(s+1) may go
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_P]));  // dV(s) and then S^T(s+1) may go
         // ---- dS^T = P^T (dP^T - D), bf16 over RP + 64g (for dK), then into
         // shared memory (for dQ)
         got = tc::mbar_wait(tc::smem_addr(&bar[B_DP]), ts & 1, abort, kTimeoutNs);
@@ -475,7 +476,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
         tc::tmem_st32(tP, dk);
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_DS]));  // dK(s) may go
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_DS]));  // dK(s) may go
         // the shared-memory dS^T buffer is free: d 128, the dq warps' staging
         // of step s-1 has been reduced out of it; d 64, dQ(s-1) has read it
         got = ts == 0 || tc::mbar_wait(tc::smem_addr(&bar[D == 128 ? B_SF : B_DQ]), (ts - 1) & 1, abort, kTimeoutNs);
@@ -487,7 +489,8 @@ __device__ __forceinline__ void pds_item(const ItemCtx& c, const BwdArgs& a, uin
             *reinterpret_cast<uint4*>(srow + unit * 16) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
         }
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_DSS]));  // dQ(s) may go
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_DSS]));  // dQ(s) may go
     }
 }
 
@@ -647,9 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mbar_init(tc::smem_addr(&bar[B_S]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_DP]), 1);
-        tc::mbar_init(tc::smem_addr(&bar[B_P]), 256);
-        tc::mbar_init(tc::smem_addr(&bar[B_DS]), 256);
-        tc::mbar_init(tc::smem_addr(&bar[B_DSS]), 256);
+        tc::mbar_init(tc::smem_addr(&bar[B_P]), 8);    // lane 0 of each P/dS warp, after its warp's stores
+        tc::mbar_init(tc::smem_addr(&bar[B_DS]), 8);
+        tc::mbar_init(tc::smem_addr(&bar[B_DSS]), 8);
         tc::mbar_init(tc::smem_addr(&bar[B_DQ]), 1);
         tc::mbar_init(tc::smem_addr(&bar[B_DQF]), 4);  // lane 0 of each dq warp
         tc::mbar_init(tc::smem_addr(&bar[B_SF]), 1);   // the dq leader

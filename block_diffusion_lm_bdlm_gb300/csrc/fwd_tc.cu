@@ -286,7 +286,8 @@ __device__ __forceinline__ void softmax_rows(const ItemCtx& c, const FwdArgs& a,
         l += sum2.x + sum2.y;
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_addr(&bar[B_P + i]));
+        __syncwarp();  // the warp's P columns are all in TMEM; one arrival per warp
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(tc::smem_addr(&bar[B_P + i]));
     }
     if (ok && c.nk > 0) {
         const bool got = tc::mbar_wait(tc::smem_addr(&bar[B_O + i]), o_count & 1, abort, kTimeoutNs);
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(tc::smem_addr(&bar[B_KVFULL + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_KVEMPTY + s]), 1);
             tc::mbar_init(tc::smem_addr(&bar[B_S + s]), 1);
-            tc::mbar_init(tc::smem_addr(&bar[B_P + s]), 128);
+            tc::mbar_init(tc::smem_addr(&bar[B_P + s]), 4);  // lane 0 of each softmax warp
             tc::mbar_init(tc::smem_addr(&bar[B_O + s]), 1);
         }
         tc::fence_barrier_init();
