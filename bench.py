@@ -49,8 +49,8 @@ UNIT = "TFLOP/s"
 # while the sources it is compiled from are unchanged (checked by hash;
 # otherwise reported as null)
 TRAFFIC = {"kernel_sources": ['block_diffusion_lm_bdlm_gb300/csrc/bwd_tc.cu', 'block_diffusion_lm_bdlm_gb300/csrc/common.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/tc_ptx.cuh', 'block_diffusion_lm_bdlm_gb300/csrc/kernels.h'],
-           "sha1": "1aafb9d1838194e57dc51a0b2ffa27d823be27f5",
-           "bytes_per_launch": 103937918720 + 60811124736,
+           "sha1": "25840ed9639536ee7e102deddc0538139b1a0c85",
+           "bytes_per_launch": 107317465088 + 62680961792,
            "note": "bwd_tc_kernel on this workload, ncu dram__bytes_read.sum + dram__bytes_write.sum"}
 
 
