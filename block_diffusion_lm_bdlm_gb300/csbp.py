@@ -30,8 +30,9 @@ The plan (the plainest reading where the pages leave a step open):
 
 The attention itself runs through an `ops` object (GpuOps: the CUDA library;
 the tests pass an implementation of the same four calls). The exchange runs
-through torch.distributed (NCCL between GPUs; gloo on CPU), or, to emulate
-all ranks in one process, through run_local.
+through torch.distributed (NCCL between GPUs; gloo with the tensors staged
+through host memory, on CPU or between processes that share a GPU), or, to
+emulate all ranks in one process, through run_local.
 """
 from __future__ import annotations
 
@@ -221,28 +222,43 @@ def rank_backward(plan: CSBPPlan, r: int, x: RankData, k_all, v_all, f: RankForw
 # ----------------------------------------------------------------------------
 # the exchange
 # ----------------------------------------------------------------------------
+def _staged(t: torch.Tensor, backend: str) -> bool:
+    """gloo moves host tensors: device tensors go through host memory."""
+    return backend != "nccl" and t.is_cuda
+
+
 def _gather_clean(t: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather of the ranks' clean shards in rank order. Under gloo a
+    device tensor is staged through host memory; 16-bit floats travel as
+    bytes (an all-gather only copies them, and gloo has no bf16 gather)."""
     import torch.distributed as dist
 
-    parts = [torch.empty_like(t) for _ in range(dist.get_world_size(group))]
-    dist.all_gather(parts, t.contiguous(), group=group)
-    return torch.cat(parts)
+    backend = dist.get_backend(group)
+    src = t.contiguous()
+    if _staged(src, backend):
+        src = src.cpu()
+    wire = src.view(torch.uint8) if src.dtype in (torch.bfloat16, torch.float16) else src
+    parts = [torch.empty_like(wire) for _ in range(dist.get_world_size(group))]
+    dist.all_gather(parts, wire, group=group)
+    out = torch.cat(parts).view(src.dtype)
+    return out.to(t.device) if out.device != t.device else out
 
 
 def _reduce_scatter_clean(share: torch.Tensor, r: int, ranks: int, group=None) -> torch.Tensor:
     """Sum the ranks' [n, ...] shares and return rows of shard r. NCCL has a
-    reduce-scatter; gloo has none, so there the sum is an all-reduce and the
-    rank keeps its rows."""
+    reduce-scatter; gloo has none, so there the sum is an all-reduce (of a
+    host copy when the shares live on a device) and the rank keeps its rows."""
     import torch.distributed as dist
 
     s = share.shape[0] // ranks
-    if dist.get_backend(group) == "nccl":
+    backend = dist.get_backend(group)
+    if backend == "nccl":
         out = torch.empty((s,) + tuple(share.shape[1:]), dtype=share.dtype, device=share.device)
         dist.reduce_scatter_tensor(out, share.contiguous(), op=dist.ReduceOp.SUM, group=group)
         return out
-    total = share.clone()
+    total = share.cpu() if _staged(share, backend) else share.clone()
     dist.all_reduce(total, op=dist.ReduceOp.SUM, group=group)
-    return total[r * s:(r + 1) * s].contiguous()
+    return total[r * s:(r + 1) * s].contiguous().to(share.device)
 
 
 def run_rank(plan: CSBPPlan, x: RankData, ops, group=None) -> Tuple[RankForward, RankGrads]:
