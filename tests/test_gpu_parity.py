@@ -203,7 +203,7 @@ def test_running_merge_in_forward(bd, n, block, H, Hk, d, shards, o_dtype):
 # the merged forward's o and lse; shares of dq sum to the full dq
 SHARDED = [
     # n, block, H, Hk, d, shards
-    (256, 16, 2, 2, 64, 2),    # the tiny workload's shape and split (warp-level kernel)
+    (256, 16, 2, 2, 64, 2),    # the tiny workload's shape and split (d 64)
     (320, 32, 8, 2, 128, 3),   # uneven shards, not block-aligned
     (96, 16, 4, 1, 128, 8),    # windows shorter than one block
     (200, 8, 3, 3, 64, 3),     # odd heads, ragged
@@ -344,7 +344,7 @@ def test_row_range_by_key_window_tasks(bd, n, block, H, Hk, d):
 RAGGED = [
     # n, block, H, Hk, d
     (100, 16, 2, 1, 128),   # 6 whole blocks + 4 rows
-    (70, 32, 4, 2, 64),     # warp-level backward
+    (70, 32, 4, 2, 64),     # d 64 backward
     (45, 8, 3, 3, 128),
     (37, 64, 2, 2, 128),    # B > n: one short block per half
     (129, 128, 2, 1, 128),  # one whole block and one row
@@ -577,7 +577,7 @@ TASK_BWD_CASES = [
     # sequence clean lengths, block, H, Hk, d
     ((300, 200), 32, 4, 2, 128),
     ((129, 70, 256), 48, 2, 1, 128),  # B divides none of them
-    ((150, 64), 16, 4, 4, 64),        # warp-level backward
+    ((150, 64), 16, 4, 4, 64),        # d 64 backward
 ]
 
 
@@ -770,3 +770,48 @@ def test_block_groups_with_a_short_last_block(bd, n, block, H, Hk, d, groups):
             check_grad(host(dv), r["dv"], f"group {order} dv")
             pad_k = torch.from_numpy(kpos < 0).cuda()
             assert torch.all(dq[~real] == 0) and torch.all(dk[pad_k] == 0) and torch.all(dv[pad_k] == 0)
+
+
+def offset_moves(q, k, scale, n, block, G):
+    """Moves of the forward's lazy offset after an item's first 128-key tile,
+    replayed on the host for the last clean row of every head: the offset
+    moves when a tile's maximum log2 score exceeds it by more than 8."""
+    row, moves = n - 1, 0
+    for h in range(q.shape[1]):
+        s = q[row, h] @ k[:(row // block + 1) * block, h // G].T * scale / np.log(2.0)
+        m = -np.inf
+        for t in range(0, len(s), 128):
+            mx = s[t:t + 128].max()
+            if mx > m + 8:
+                moves += t > 0
+                m = mx
+    return moves
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,top", [(320, 32, 4, 2, 128, 6.0), (400, 8, 2, 1, 64, 8.0),
+                                                  (512, 64, 4, 4, 128, 3.0)])
+def test_growing_scores_move_the_softmax_offset(bd, n, block, H, Hk, d, top):
+    """Keys whose magnitude grows along the sequence (k row t scaled by
+    1 + top * t / 2n, q and k drawn with std 2) give later key tiles much
+    larger row maxima, so the forward's running offset moves and O is
+    rescaled in TMEM on many key tiles after an item's first, with scores
+    spanning over a hundred units of log2 (3 to 7 moves on the last clean
+    rows over ten seeds of each case). v is scaled back to std 0.5, so that
+    o stays in the range the max-abs tolerance is stated for (bf16 rounding
+    of |o| near 8 alone is up to 0.03). o, lse and the gradients against the
+    float64 oracle on the same bf16 values."""
+    w, x = gen(n, block, H, Hk, d, seed=n + 5, std=2.0)
+    L = x.k.shape[0]
+    ramp = 1.0 + top * torch.arange(L, device=x.k.device, dtype=torch.float32) / L
+    x.k.copy_((x.k.float() * ramp[:, None, None]).to(x.k.dtype))
+    x.v.copy_((x.v.float() * 0.25).to(x.v.dtype))
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block)
+    torch.cuda.synchronize()
+    r = ref_full(x, w)
+    assert offset_moves(host(x.q), host(x.k), w.scale, n, block, H // Hk) > 0  # the case is what it claims
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
