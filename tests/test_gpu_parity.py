@@ -815,3 +815,25 @@ def test_growing_scores_move_the_softmax_offset(bd, n, block, H, Hk, d, top):
     check_grad(host(dq), r["dq"], "dq")
     check_grad(host(dk), r["dk"], "dk")
     check_grad(host(dv), r["dv"], "dv")
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,scale", [(160, 16, 4, 2, 128, 0.3), (96, 32, 2, 1, 64, 0.05)])
+def test_explicit_softmax_scale(bd, n, block, H, Hk, d, scale):
+    """A softmax scale other than 1/sqrt(d) reaches the forward's exponent,
+    the backward's recomputed P and dS, and the dq conversion: o, lse and
+    the gradients against the oracle taken with the same scale. A scale <= 0
+    means 1/sqrt(d): bit-identical to the default call."""
+    w, x = gen(n, block, H, Hk, d, seed=n + 11)
+    o, lse = bd.bdlm_attn_fwd(x.q, x.k, x.v, block, softmax_scale=scale)
+    dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k, x.v, o, lse, x.do, block, softmax_scale=scale)
+    torch.cuda.synchronize()
+    r = oracle.bdlm_attention(host(x.q), host(x.k), host(x.v), block, scale, do=host(x.do))
+    check_o(host(o), r["o"])
+    check_lse(host(lse), r["lse"])
+    check_grad(host(dq), r["dq"], "dq")
+    check_grad(host(dk), r["dk"], "dk")
+    check_grad(host(dv), r["dv"], "dv")
+    o0, lse0 = bd.bdlm_attn_fwd(x.q, x.k, x.v, block)
+    o1, lse1 = bd.bdlm_attn_fwd(x.q, x.k, x.v, block, softmax_scale=-1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(lse0, lse1)
