@@ -837,3 +837,52 @@ def test_explicit_softmax_scale(bd, n, block, H, Hk, d, scale):
     o1, lse1 = bd.bdlm_attn_fwd(x.q, x.k, x.v, block, softmax_scale=-1.0)
     torch.cuda.synchronize()
     assert torch.equal(o0, o1) and torch.equal(lse0, lse1)
+
+
+@pytest.mark.parametrize("n,block,H,Hk,d,shards", [(320, 32, 4, 2, 128, 3), (192, 16, 2, 1, 64, 4)])
+def test_sharded_with_growing_scores(bd, n, block, H, Hk, d, shards):
+    """Sharp scores across shards (keys growing along the sequence, as in
+    test_growing_scores_move_the_softmax_offset): the windows' partial lse
+    values differ by tens of log2 units row by row, so the LSE merge (of
+    bf16 partials) and the forward's running merge (fp32) weigh partials
+    whose weights differ by many orders of magnitude; then the sharded
+    backward with the merged o and lse. All against the oracle."""
+    w, x = gen(n, block, H, Hk, d, seed=7 * n + shards, std=2.0)
+    L = x.k.shape[0]
+    ramp = 1.0 + 6.0 * torch.arange(L, device=x.k.device, dtype=torch.float32) / L
+    x.k.copy_((x.k.float() * ramp[:, None, None]).to(x.k.dtype))
+    x.v.copy_((x.v.float() * 0.25).to(x.v.dtype))
+    q64, k64, v64, do64 = host(x.q), host(x.k), host(x.v), host(x.do)
+    full = oracle.bdlm_attention(q64, k64, v64, block, w.scale, do=do64)
+    windows = synth.shard_bounds(n, shards) + [(n, 2 * n)]
+    parts, lses = [], []
+    o_run = torch.empty(x.q.shape, dtype=torch.float32, device="cuda")
+    lse_run = torch.empty((H, 2 * n), dtype=torch.float32, device="cuda")
+    for i, (lo, hi) in enumerate(windows):
+        kw, vw = x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous()
+        po, pl = bd.bdlm_attn_fwd(x.q, kw, vw, block, part=bd.Partial.window(lo, hi))
+        parts.append(po)
+        lses.append(pl)
+        bd.bdlm_attn_fwd(x.q, kw, vw, block, part=bd.Partial.window(lo, hi, accumulate=i > 0), out=o_run, lse=lse_run)
+    spread = torch.stack(lses)
+    fin = torch.isfinite(spread)
+    gap = (spread.masked_fill(~fin, -1e30).amax(0) - spread.masked_fill(~fin, 1e30).amin(0))[fin.sum(0) > 1]
+    assert gap.max().item() / math.log(2.0) > 20  # partials of one row many orders of magnitude apart
+    mo, ml = bd.bdlm_lse_merge(parts, lses)
+    torch.cuda.synchronize()
+    check_o(host(mo), full["o"], "merged o")
+    check_lse(host(ml), full["lse"], "merged lse")
+    check_o(host(o_run), full["o"], "running-merge o")
+    check_lse(host(lse_run), full["lse"], "running-merge lse")
+    dq_sum = torch.zeros(2 * n, H, d, dtype=torch.float32, device="cuda")
+    dk_cat, dv_cat = torch.empty_like(x.k), torch.empty_like(x.v)
+    for lo, hi in windows:
+        dq, dk, dv = bd.bdlm_attn_bwd(x.q, x.k[lo:hi].contiguous(), x.v[lo:hi].contiguous(), mo, ml, x.do, block,
+                                      part=bd.Partial.window(lo, hi))
+        dq_sum += dq.float()
+        dk_cat[lo:hi] = dk
+        dv_cat[lo:hi] = dv
+    torch.cuda.synchronize()
+    check_grad(host(dq_sum), full["dq"], "sum of dq shares")
+    check_grad(host(dk_cat), full["dk"], "dk over all shards")
+    check_grad(host(dv_cat), full["dv"], "dv over all shards")
