@@ -408,7 +408,7 @@ def bdlm_attn_fwd_noalloc(q, k, v, block: int, *, L: Optional[int] = None, cu_se
     to allocate nothing at all). Problems found on the device (a malformed
     cu_seqlens or block list) leave o and lse unwritten and are reported by
     bdlm_read_error(None); check=True synchronises the stream after the call
-    and raises BDLMError for them (not allowed under stream capture)."""
+    and raises BDLMError for them."""
     lib = load_library()
     for nm, t in (("q", q), ("k", k), ("v", v)):
         _bf16_cuda(nm, t)

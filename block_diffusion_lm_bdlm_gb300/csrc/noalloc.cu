@@ -1,10 +1,9 @@
 // noalloc.cu - bdlm_attn_fwd_noalloc: the forward without a caller workspace.
 //
 // Some callers cannot allocate device memory at the point where they run
-// attention: code being captured into a CUDA graph (cudaMalloc is not allowed
-// during stream capture), plugins hosted by a framework or server that owns
-// every device allocation and hands out no allocator, and real-time services
-// that forbid allocation after start-up. They still own and pass q, k, v, o
+// attention: plugins hosted by a framework or server that owns every device
+// allocation and hands out no allocator, and real-time services that forbid
+// allocation after start-up. They still own and pass q, k, v, o
 // and lse; the forward's own scratch (the tile table, the work counter and
 // the device error word) lives here instead, in a fixed array that every GPU
 // which loads this library holds until the process exits.

@@ -36,8 +36,7 @@
  *     kernels on `stream`, with every host-side value (task records, partial
  *     pointer lists, tensor maps) in kernel parameters, so they can be
  *     captured into a CUDA graph and replayed on new contents of the same
- *     buffers. (bdlm_attn_fwd_noalloc must have run once on the device
- *     before a capture; bdlm_read_error synchronises and cannot be captured.)
+ *     buffers. (bdlm_read_error synchronises and cannot be captured.)
  */
 #ifndef BDLM_H
 #define BDLM_H
@@ -163,10 +162,9 @@ BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o,
 
 /*
  * bdlm_attn_fwd_noalloc - the forward for callers that cannot allocate device
- * memory where they call it: code under CUDA stream capture (cudaMalloc is not
- * allowed there), plugins whose host framework owns every device allocation,
- * services that forbid allocation after start-up. (The paper has no
- * counterpart; this is a library convenience.)
+ * memory where they call it: plugins whose host framework owns every device
+ * allocation, services that forbid allocation after start-up. (The paper has
+ * no counterpart; this is a library convenience.)
  *
  * Same arguments and results as bdlm_attn_fwd, minus the workspace: the
  * forward's scratch (tile table, work counter, device error word) lives in a
@@ -176,10 +174,9 @@ BDLM_API int bdlm_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * (about 2.5 million rows for one sequence) the call returns
  * BDLM_ERR_WORKSPACE and launches nothing; use bdlm_attn_fwd then.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. The address is kept together with the CUDA context it belongs to
- * and looked up again when the device's current context changes (e.g. after
- * cudaDeviceReset); that later lookup is again not allowed under capture.
+ * device, with that device current). The address is kept together with the
+ * CUDA context it belongs to and looked up again when the device's current
+ * context changes (e.g. after cudaDeviceReset).
  * Every call on a device shares the one array and each call clears the parts
  * that must start at zero; calls whose execution overlaps on the GPU (other
  * streams, or other host threads) race on it, so order them.

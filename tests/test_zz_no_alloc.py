@@ -1,5 +1,5 @@
 """bdlm_attn_fwd_noalloc: the forward for callers that cannot allocate device
-memory (stream capture, framework-owned memory, no allocation after start-up).
+memory (framework-owned memory, no allocation after start-up).
 
 It is called here through the C ABI with caller-owned outputs only, and its
 results are checked against bdlm_attn_fwd (which takes a caller workspace) and
